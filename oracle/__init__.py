@@ -1,0 +1,142 @@
+"""ORACLE -- test infrastructure, not part of the product.
+
+Plain, slow, obviously correct CPU implementations of what the decode path
+computes, used only by tests/, the smoke check and the bench's CPU-baseline
+(and `--impl reference`) legs. The CUDA library never imports, links or calls
+anything here, and nothing here imports the CUDA library: the two share no
+code. Only the seeded input generators are common to both sides.
+
+Contents:
+  decode_ref.c   fp64 paged GQA decode from its definition (POSIX threads).
+  plan_ref.py    the dynamic (load-balanced) and static split-KV tile plans.
+  merge_ref.py   partial softmax states and their log-sum-exp merge.
+
+Every function here has pins in tests/ (closed forms, brute force,
+invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "decode_ref.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle_decode.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile decode_ref.c with gcc (plain C, -O2, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Load a compiled oracle library (the default one, or a test's variant)."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, f64 = ctypes.c_int32, ctypes.c_double
+    lib.oracle_paged_decode.restype = ctypes.c_int
+    lib.oracle_paged_decode.argtypes = [i32, i32, i32, i32, P, P, P, i32, f64, f64,
+                                        P, i32, P, f64, P, P, i32]
+    lib.oracle_bf16_to_f64.restype = f64
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_e4m3_to_f64.restype = f64
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_num_cpus.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def num_cpus() -> int:
+    return int(_load().oracle_num_cpus())
+
+
+def bf16_to_f64(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f64(bits & 0xFFFF))
+
+
+def e4m3_to_f64(byte: int) -> float:
+    return float(_load().oracle_e4m3_to_f64(byte & 0xFF))
+
+
+def _as_u16(x) -> np.ndarray:
+    """bf16 payload as uint16 bits (accepts a torch bf16 tensor or uint16 array)."""
+    if hasattr(x, "dtype") and str(getattr(x, "dtype")) == "torch.bfloat16":
+        import torch
+        return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+    a = np.ascontiguousarray(np.asarray(x))
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 data must be given as uint16 bits")
+    return a
+
+
+def _as_np(x, dtype) -> np.ndarray:
+    if hasattr(x, "numpy") and not isinstance(x, np.ndarray):
+        x = x.contiguous().numpy()
+    a = np.ascontiguousarray(np.asarray(x))
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def paged_decode(q, k_cache, v_cache, block_table, seq_lens, *, num_kv_heads: int,
+                 softmax_scale: float, kv_is_fp8: bool = False, k_scale: float = 1.0,
+                 v_scale: float = 1.0, num_threads: int = 0, lib=None):
+    """fp64 decode attention. Returns (out [B][H_q][D] f64, lse [B][H_q] f64).
+
+    q: bf16 [B][H_q][D]; k_cache/v_cache: bf16 or e4m3 bytes (uint8)
+    [num_blocks][H_kv][64][D]; block_table int32 [B][max_blocks];
+    seq_lens int32 [B].
+    """
+    lib = _load() if lib is None else lib
+    qb = _as_u16(q)
+    if kv_is_fp8:
+        kb, vb = _as_np(k_cache, np.uint8), _as_np(v_cache, np.uint8)
+    else:
+        kb, vb = _as_u16(k_cache), _as_u16(v_cache)
+    bt = _as_np(block_table, np.int32)
+    sl = _as_np(seq_lens, np.int32)
+    B, hq, D = qb.shape
+    if kb.shape[1] != num_kv_heads or kb.shape[2] != 64 or kb.shape[3] != D:
+        raise ValueError("k_cache must be [num_blocks][H_kv][64][D]")
+    if kb.shape != vb.shape or bt.shape[0] != B or sl.shape != (B,):
+        raise ValueError("shape mismatch")
+    out = np.zeros((B, hq, D), dtype=np.float64)
+    lse = np.zeros((B, hq), dtype=np.float64)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib.oracle_paged_decode(B, hq, num_kv_heads, D, ptr(qb), ptr(kb), ptr(vb),
+                                 1 if kv_is_fp8 else 0, float(k_scale), float(v_scale),
+                                 ptr(bt), bt.shape[1], ptr(sl), float(softmax_scale),
+                                 ptr(out), ptr(lse), int(num_threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_paged_decode failed with code {rc}")
+    return out, lse
+
+
+def decode_workload(w, num_threads: int = 0, lib=None):
+    """Convenience: run the oracle on a workloads.Workload-like object."""
+    return paged_decode(w.q, w.k_cache, w.v_cache, w.block_table, w.seq_lens,
+                        num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
+                        kv_is_fp8=(w.kv_dtype == "fp8_e4m3"), k_scale=w.k_scale,
+                        v_scale=w.v_scale, num_threads=num_threads, lib=lib)
