@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of mixed-length paged GQA decode attention on GB300.
+
+One step = the whole hot path on one batch already resident in HBM: the
+device tile planner, the persistent split-KV attention kernel and the LSE
+merge kernel, launched through the C ABI on one stream. Reported `value` is
+achieved HBM GB/s = algorithmic bytes (KV of the actual tokens + Q + O) per
+step / device time per step, summed over ranks (weak scaling: every rank
+runs its own replica of the batch). The default workload is the skewed
+batch (1 x 131072 + 31 x 4096 KV tokens, 64 q / 8 kv heads, head_dim 128,
+bf16 KV in 64-token blocks).
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   (the fp64 CPU oracle, timed on host cores)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak), mixed-length paged GQA"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD_TEXT = {
+    "tiny": "tiny: 4 seqs KV {37,64,200,1000}, 8 q / 1 kv heads, d128, bf16 KV",
+    "uniform": "uniform: 64 seqs x 512 KV tokens, 64 q / 8 kv heads, d128, bf16 KV",
+    "skewed": "skewed: 1 x 131072 + 31 x 4096 KV tokens, 64 q / 8 kv heads, d128, bf16 KV",
+    "skewed_fp8": "skewed FP8: 1 x 131072 + 31 x 4096 KV tokens, 64 q / 8 kv heads, d128, "
+                  "fp8_e4m3 KV (per-tensor scales), bf16 q/out",
+    "random_mixed": "random mixed: 256 seqs, KV lengths log-uniform in [16, 65536], "
+                    "64 q / 8 kv heads, d128, bf16 KV",
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["hpc", "reference"], default="hpc")
+    ap.add_argument("--config", default="skewed", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--no-static", action="store_true", help="skip the static split-KV ablation")
+    ap.add_argument("--static-sweep", default="1,2,4,8,16,32",
+                    help="split counts timed for the static ablation ('' = rule only)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
+    ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in d and d[k]:
+                return float(d[k]), "measured (MEASURED_PEAKS.json)"
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for name in ("attn_kernel.cu", "hpc_internal.h"):
+        with open(os.path.join(ROOT, "paged_gqa_decode_hpc_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_name):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"attn_kernel_{config_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_digest():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle leg
+def oracle_sample(w, budget_s=4.0):
+    """A bounded sample of the workload for the oracle: whole sequences, taken
+    in order until the estimated fp64 CPU time reaches `budget_s`."""
+    import oracle
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+    lens = w.seq_lens.tolist()
+    # calibrate on the shortest non-empty sequences (about 0.2 s of work)
+    order = sorted(range(len(lens)), key=lambda b: lens[b])
+    calib, tok = [], 0
+    for b in order:
+        if lens[b] > 0:
+            calib.append(b)
+            tok += lens[b]
+        if tok > 20000:
+            break
+    t0 = time.perf_counter()
+    oracle.decode_workload(_subset(w, calib))
+    rate = tok / max(time.perf_counter() - t0, 1e-6)  # tokens / s
+    chosen, est = [], 0.0
+    for b in range(len(lens)):
+        cost = lens[b] / rate
+        if chosen and est + cost > budget_s:
+            continue
+        chosen.append(b)
+        est += cost
+    return _subset(w, chosen), chosen
+
+
+def _subset(w, seqs):
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+    import torch
+    idx = torch.tensor(seqs, dtype=torch.long)
+    return W.Workload(w.config_name, w.seq_lens[idx].clone(), w.block_table[idx].clone(),
+                      w.q[idx].clone(), w.k_cache, w.v_cache, w.k_scale, w.v_scale, w.kv_dtype,
+                      w.softmax_scale, w.num_q_heads, w.num_kv_heads)
+
+
+def time_oracle(sample, reps):
+    import oracle
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.decode_workload(sample)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+# ------------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+    w = W.make_workload(args.config)
+    budget = max(0.5, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    sample, seqs = oracle_sample(w, budget_s=budget)
+    time_oracle(sample, args.warmup)
+    times = time_oracle(sample, args.steps)
+    step_s = statistics.mean(times)
+    gbs = sample.algorithmic_bytes() / step_s / 1e9
+    desc = (f"{len(seqs)} of {w.num_seqs} sequences ({int(sample.seq_lens.sum())} of "
+            f"{int(w.seq_lens.sum())} KV tokens) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, the pages' shapes)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "sample": desc},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_cpus(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    emit(line, args)
+
+
+def emit(line, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.json_out:
+        with open(args.json_out, "a") as f:
+            f.write(s + "\n")
+
+
+# ---------------------------------------------------------------- hpc arm
+def run_hpc(args, ws, rank, local):
+    import torch
+    import paged_gqa_decode_hpc_gb300 as hpc
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
+    hpc.load_library()
+    dev = torch.device("cuda", local)
+    w = W.make_workload(args.config)
+    B, hq, hkv = w.num_seqs, w.num_q_heads, w.num_kv_heads
+    fp8 = w.kv_dtype == "fp8_e4m3"
+    q, kc, vc = w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev)
+    bt, sl = w.block_table.to(dev), w.seq_lens.to(dev)
+    out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+    num_sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(B, num_sms, hq)
+    stream = torch.cuda.current_stream()
+    nbytes = w.algorithmic_bytes()
+    flush = None if args.no_flush else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        if flush is not None:
+            flush.fill_(1)
+
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)  # materialise the handle
+        return e
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+            hpc.hpc_decode_plan_set_timing_events(plan, evs[1], evs[2], evs[3])
+        hpc.hpc_decode_plan_device(sl, num_sms, plan, stream)
+        hpc.hpc_decode_attn(q, kc, vc, bt, sl, plan, out, lse, stream=stream,
+                            k_scale=w.k_scale, v_scale=w.v_scale)
+        if evs:
+            hpc.hpc_decode_plan_set_timing_events(plan)
+
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    assert hpc.hpc_decode_plan_status(plan) == 0, "device checks fired during warm-up"
+    ev = [[mk() for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush_l2()
+        step(ev[i])
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    if hpc.hpc_decode_plan_status(plan) != 0:
+        raise SystemExit("device checks fired during the timed steps")
+    if not torch.isfinite(out.float()).all():
+        raise SystemExit("non-finite output")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    plan_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    ms = statistics.mean(step_ms)
+    ms_all = max_over_ranks(ws, ms)
+    value = ws * nbytes / (ms_all * 1e-3) / 1e9
+
+    peak, peak_src = measured_peak_gbs()
+    attn_mean = statistics.mean(attn_ms)
+    achieved = nbytes / (attn_mean * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_all, 5),
+        "us_per_step": round(ms_all * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V, shuffled block table; the pages' shapes)",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.config], "num_seqs": B,
+            "kv_tokens": int(w.seq_lens.sum()), "num_sms": num_sms,
+            "algorithmic_bytes_per_step": nbytes,
+            "l2": ("flushed between steps (write of 2x L2)" if flush is not None
+                   else "not flushed"),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+        },
+        "breakdown_us": {"device_plan": round(statistics.mean(plan_ms) * 1e3, 2),
+                         "attention": round(attn_mean * 1e3, 2),
+                         "merge": round(statistics.mean(merge_ms) * 1e3, 2),
+                         "step_median": round(statistics.median(step_ms) * 1e3, 2),
+                         "step_min": round(min(step_ms) * 1e3, 2)},
+        "frac_of_peak_step": round(value / ws / peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(args.config), "kernel": "attn_kernel",
+                     "peak_source": peak_src,
+                     "bytes_per_launch": nbytes},
+        "gpu_launches": 3 * args.steps,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if clocks:
+        line["clocks"] = clocks
+
+    # ---- static split-KV ablation (attention + merge, host-built plans)
+    if not args.no_static:
+        def time_plan(p, steps):
+            es = [[mk(), mk()] for _ in range(steps)]
+            for _ in range(2):
+                flush_l2()
+                hpc.hpc_decode_attn(q, kc, vc, bt, sl, p, out, lse, stream=stream,
+                                    k_scale=w.k_scale, v_scale=w.v_scale)
+            torch.cuda.synchronize()
+            for e in es:
+                flush_l2()
+                e[0].record(stream)
+                hpc.hpc_decode_attn(q, kc, vc, bt, sl, p, out, lse, stream=stream,
+                                    k_scale=w.k_scale, v_scale=w.v_scale)
+                e[1].record(stream)
+            torch.cuda.synchronize()
+            assert hpc.hpc_decode_plan_status(p) == 0
+            return statistics.mean(e[0].elapsed_time(e[1]) for e in es) * 1e3
+
+        n_st = max(3, min(args.steps, 10))
+        lens = w.seq_lens.tolist()
+        with hpc.hpc_decode_plan(lens, num_sms) as pd:
+            dyn_us = time_plan(pd, n_st)
+        with hpc.hpc_decode_plan_static(lens, num_sms, hkv, 0) as ps:
+            rule_S = int(hpc.hpc_decode_plan_export(ps)[7])
+            st_us = time_plan(ps, n_st)
+        sweep = {}
+        for s in [int(x) for x in args.static_sweep.split(",") if x.strip()]:
+            with hpc.hpc_decode_plan_static(lens, num_sms, hkv, s) as ps:
+                sweep[s] = round(time_plan(ps, n_st), 2)
+        best = min(sweep.values()) if sweep else st_us
+        line["static_ablation"] = {
+            "dynamic_attn_merge_us": round(dyn_us, 2), "static_rule_splits": rule_S,
+            "static_rule_us": round(st_us, 2), "static_sweep_us": sweep,
+            "speedup_vs_static_rule": round(st_us / dyn_us, 3),
+            "speedup_vs_best_static": round(best / dyn_us, 3)}
+
+    # ---- end to end through the public API, host buffers
+    if not args.no_e2e:
+        q_h = w.q.pin_memory()
+        sl_h = w.seq_lens.pin_memory()
+        bt_h = w.block_table.pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = q_h.numel() * 2 + sl_h.numel() * 4 + bt_h.numel() * 4
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+        def e2e_step():
+            q.copy_(q_h, non_blocking=True)
+            sl.copy_(sl_h, non_blocking=True)
+            bt.copy_(bt_h, non_blocking=True)
+            hpc.hpc_decode_plan_device(sl, num_sms, plan, stream)
+            hpc.hpc_decode_attn(q, kc, vc, bt, sl, plan, out, lse, stream=stream,
+                                k_scale=w.k_scale, v_scale=w.v_scale)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            flush_l2()
+            e2e_step()
+        es = [[mk(), mk()] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(ws)
+        for e in es:
+            flush_l2()
+            e[0].record(stream)
+            e2e_step()
+            e[1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(ws, statistics.mean(a.elapsed_time(b) for a, b in es))
+        line["e2e"] = {"value": round(ws * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "us_per_step": round(e2e_ms * 1e3, 2),
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        line["gpu_launches"] += 3 * args.steps
+
+    # ---- fp64 CPU oracle on host cores (rank 0, N = 1 only)
+    if not args.no_cpu_baseline and ws == 1 and rank == 0:
+        import oracle
+        sample, seqs = oracle_sample(w, budget_s=6.0)
+        times = time_oracle(sample, 3)
+        t = statistics.mean(times)
+        line["cpu_baseline"] = {
+            "value": round(sample.algorithmic_bytes() / t / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_cpus(), "kind": "oracle",
+            "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
+                      f"{int(w.seq_lens.sum())} KV tokens), mean of 3 runs, {t:.2f} s each"}
+
+    plan.destroy()
+    if rank == 0:
+        emit(line, args)
+
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_hpc(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            if dist.is_initialized():
+                dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,257 @@
+/*
+ * hpc_decode.h -- C ABI of libhpc_decode.so: mixed-length paged GQA decode
+ * attention for NVIDIA GB300 (sm_103a), one GPU per process.
+ *
+ * The operation ("vLLM x HPC-Ops: High-Performance Attention and MoE
+ * Backends", section "Attention Backend: Dynamic Load-Balanced Scheduling"):
+ * each decode step, every sequence's KV cache is cut into uniform 64-token
+ * tiles, the tiles are spread by actual work over the CTAs of a persistent
+ * grid, each CTA runs split-KV attention of one query token per sequence over
+ * its tiles, and a merge pass combines the partial softmax states. The KV
+ * cache is paged in 64-token blocks and may be fp8_e4m3 (section "Using
+ * HPC-Ops Backends in vLLM": --block-size 64, --kv-cache-dtype fp8_e4m3).
+ * The model shape is GQA with 8 query heads per KV head and head_dim 128
+ * (24-ai.news page, Hy3 paragraph: 64 query heads, 8 KV heads, head dim 128).
+ *
+ * For sequence b, query head j (kv head h = j / 8), N = seq_lens[b]:
+ *   s_t = softmax_scale * q[b][j] . k_t,     t < N
+ *   out[b][j] = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m),  m = max_t s_t
+ *   lse[b][j] = m + ln(sum_t exp(s_t - m))                    (natural log)
+ * Token t of sequence b is slot t % 64 of physical block block_table[b][t/64].
+ * A sequence of length 0 yields out = 0 and lse = -inf.
+ *
+ * Conventions for every call:
+ *   - Return value: an hpc_status. Nothing throws across the ABI. On failure
+ *     hpc_last_error() returns a message for the calling thread.
+ *   - Device pointers are CUDA device (or managed) memory of the current
+ *     device; "host" pointers are ordinary CPU memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *     that take a stream only enqueue work and never synchronise it, unless
+ *     stated otherwise.
+ *   - The caller owns every tensor. A plan owns its device work list, its
+ *     partial-result workspace and its device error word; destroy frees them.
+ *   - There is no CPU fallback: without a usable CUDA device the calls
+ *     return HPC_ERR_CUDA.
+ */
+#ifndef HPC_DECODE_H
+#define HPC_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HPC_OK = 0,
+  HPC_ERR_INVALID_ARG = 1,   /* null pointer, bad shape/stride/dtype, bad length */
+  HPC_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  HPC_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
+  HPC_ERR_OOM = 4,           /* device or host allocation failed */
+  HPC_ERR_DEVICE_CHECK = 5   /* a kernel's own bounds/consistency check fired */
+} hpc_status;
+
+typedef enum {
+  HPC_BF16 = 0,
+  HPC_FP8_E4M3 = 1,
+  HPC_F32 = 2,
+  HPC_I32 = 3
+} hpc_dtype;
+
+/*
+ * Strided tensor descriptor. `shape`/`stride` hold `ndim` entries (outermost
+ * first); strides are in elements. `scale` is the per-tensor dequantisation
+ * scale of an FP8 K or V cache (value = e4m3(byte) * scale); it is ignored for
+ * every other tensor.
+ */
+typedef struct {
+  void* data;
+  int32_t dtype; /* hpc_dtype */
+  int32_t ndim;
+  int64_t shape[4];
+  int64_t stride[4];
+  float scale;
+} hpc_tensor;
+
+/* Opaque plan handle: the tile -> CTA work list of one decode step. */
+typedef struct hpc_plan_s* hpc_plan_t;
+
+/* Plan kinds reported in word 1 of an exported plan. */
+#define HPC_PLAN_DYNAMIC 0
+#define HPC_PLAN_STATIC 1
+
+/* Segment flag: the segment covers every tile of its sequence. */
+#define HPC_SEG_WHOLE 1
+
+/*
+ * hpc_decode_plan -- the per-step load-balanced tile scheduler (section
+ * "Attention Backend: Dynamic Load-Balanced Scheduling": uniform 64-token
+ * tiles, assigned to CTAs by actual work; the 24-ai.news page: tiles spread
+ * in proportion to each sequence's current length).
+ *
+ * Rule (every tile costs one unit; no sorting): sequence b has
+ * n_b = ceil(seq_lens[b] / 64) tiles; tiles are flattened in sequence order,
+ * T = sum n_b, P = min(num_sms, T) parts; part p owns flattened tiles
+ * [floor(p*T/P), floor((p+1)*T/P)). A segment is the part's intersection with
+ * one sequence, listed by part then sequence; its partial-result slot is its
+ * index in that list. One part runs on one CTA of the persistent grid.
+ *
+ *   seq_lens  host int32 [num_seqs], each >= 0 (else HPC_ERR_INVALID_ARG)
+ *   num_seqs  >= 0
+ *   num_sms   > 0: CTAs of the persistent grid (normally the SM count)
+ *   plan_out  receives a new plan; the caller destroys it
+ * The work list is uploaded to the current device before returning
+ * (synchronous). The plan's capacity is exactly this step's size.
+ */
+hpc_status hpc_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                           hpc_plan_t* plan_out);
+
+/*
+ * hpc_decode_plan_create -- an empty dynamic plan able to hold any step with
+ * at most `max_seqs` sequences on `num_sms` CTAs; fill it with
+ * hpc_decode_plan_device (or hpc_decode_plan_update) every step. All device
+ * memory, including the partial workspace for `num_q_heads` query heads of
+ * head_dim 128, is allocated here, so later calls allocate nothing and may be
+ * captured in a CUDA graph.
+ */
+hpc_status hpc_decode_plan_create(int32_t max_seqs, int32_t num_sms, int32_t num_q_heads,
+                                  hpc_plan_t* plan_out);
+
+/*
+ * hpc_decode_plan_device -- the same rule as hpc_decode_plan, computed on the
+ * GPU from device lengths, into a plan from hpc_decode_plan_create. No host
+ * synchronisation; the result is bit-identical to the host plan of the same
+ * lengths (see hpc_decode_plan_export).
+ *   seq_lens_dev  device int32 [num_seqs]; a negative length makes the device
+ *                 check fire (reported by hpc_decode_plan_status), and the
+ *                 plan is then empty.
+ *   num_seqs      <= the plan's max_seqs;   num_sms <= the plan's num_sms.
+ */
+hpc_status hpc_decode_plan_device(const int32_t* seq_lens_dev, int32_t num_seqs,
+                                  int32_t num_sms, hpc_plan_t plan, void* stream);
+
+/*
+ * hpc_decode_plan_update -- the host planner into an existing plan (same
+ * capacity rules as hpc_decode_plan_device); the upload is enqueued on
+ * `stream` from a plan-owned pinned buffer, so the previous step's kernels
+ * must not still read it (they are ordered on the same stream).
+ */
+hpc_status hpc_decode_plan_update(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                  hpc_plan_t plan, void* stream);
+
+/*
+ * hpc_decode_plan_static -- the static even split-KV schedule, the baseline
+ * the pages compare against (same section: "static split-KV"; the 24-ai.news
+ * page: it assumes uniform lengths). Sequence b is cut into S splits
+ * [floor(i*n_b/S), floor((i+1)*n_b/S)), empty splits dropped; each split runs
+ * on one CTA per KV head (grid = splits x num_kv_heads, not persistent).
+ * num_splits > 0 fixes S; num_splits <= 0 uses
+ * S = clamp(ceil(2*num_sms / (num_seqs*num_kv_heads)), 1, max_b n_b).
+ * S is always clamped to [1, max_b n_b]. Upload is synchronous.
+ */
+hpc_status hpc_decode_plan_static(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                  int32_t num_kv_heads, int32_t num_splits,
+                                  hpc_plan_t* plan_out);
+
+/*
+ * hpc_decode_plan_export -- copy a plan to host memory (synchronises the
+ * device) in this canonical int32 layout:
+ *   [0] 0x48504344  [1] kind  [2] num_seqs B  [3] num_parts P  [4] num_tiles T
+ *   [5] num_segs S  [6] num_sms  [7] static split count (0 for dynamic)
+ *   part_seg_off[P + 1], seq_seg_off[B + 1],
+ *   segs[S][4] = {seq, tile_begin, tile_end, flags}   (tiles relative to seq)
+ * For a static plan part p is segment p (part_seg_off = 0..S).
+ *   buf  host int32 [cap] (may be NULL when cap == 0: only *len is written)
+ *   len  receives the number of words; HPC_ERR_INVALID_ARG if cap < *len.
+ */
+hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, int64_t* len);
+
+/*
+ * hpc_decode_plan_compute / hpc_decode_plan_static_compute -- the host
+ * planners alone: the same plans as hpc_decode_plan / hpc_decode_plan_static,
+ * written in the canonical layout of hpc_decode_plan_export into host memory.
+ * No device is touched (usable on machines without a GPU).
+ *   buf  host int32 [cap] (may be NULL when cap == 0: only *len is written)
+ *   len  receives the number of words; HPC_ERR_INVALID_ARG if cap < *len.
+ */
+hpc_status hpc_decode_plan_compute(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                   int32_t* buf, int64_t cap, int64_t* len);
+hpc_status hpc_decode_plan_static_compute(const int32_t* seq_lens, int32_t num_seqs,
+                                          int32_t num_sms, int32_t num_kv_heads,
+                                          int32_t num_splits, int32_t* buf, int64_t cap,
+                                          int64_t* len);
+
+/*
+ * hpc_decode_plan_status -- synchronise the device and read (then clear) the
+ * plan's device error word. *device_error = 0 when no kernel check fired;
+ * otherwise a bit set of HPC_DEVCHK_* values. Returns HPC_ERR_DEVICE_CHECK
+ * when the word was non-zero.
+ */
+#define HPC_DEVCHK_BAD_LENGTH 1       /* negative length, or lengths != plan */
+#define HPC_DEVCHK_BAD_BLOCK 2        /* block id outside [0, num_blocks) */
+#define HPC_DEVCHK_TABLE_TOO_SHORT 4  /* a sequence needs more than max_blocks */
+#define HPC_DEVCHK_TIMEOUT 8          /* a bounded wait gave up */
+#define HPC_DEVCHK_CAPACITY 16        /* a step larger than the plan's capacity */
+hpc_status hpc_decode_plan_status(hpc_plan_t plan, int32_t* device_error);
+
+/* hpc_decode_plan_destroy -- free a plan (NULL is a no-op). Synchronises the
+ * device first so that no enqueued kernel still reads it. */
+void hpc_decode_plan_destroy(hpc_plan_t plan);
+
+/*
+ * hpc_decode_attn -- run decode attention for one step with a plan built from
+ * the same lengths: the persistent split-KV kernel (dynamic plan) or the
+ * per-split kernel (static plan), then the log-sum-exp merge of split
+ * sequences. Softmax scale 1/sqrt(head_dim).
+ *
+ *   q            device bf16 [B][H_q][128], innermost stride 1
+ *   k_cache      device bf16 or fp8_e4m3 [num_blocks][H_kv][64][128],
+ *   v_cache      innermost stride 1, other strides multiples of 16 bytes, base
+ *                16-byte aligned (a [num_blocks][64][H_kv][128] cache passes as
+ *                a permuted view). Both must have the same dtype; FP8 caches
+ *                carry their per-tensor scale in `scale`.
+ *   block_table  device int32 [B][max_blocks], innermost stride 1; entry
+ *                [b][i] for i < ceil(seq_lens[b]/64) is a physical block id
+ *   seq_lens     device int32 [B]: the lengths the plan was built from
+ *   plan         from any hpc_decode_plan* call with num_seqs == B
+ *   out          device bf16 [B][H_q][128], innermost stride 1 (written)
+ *   lse          device f32 [B][H_q] natural-log LSE (written), or NULL
+ * Requirements: H_q == 8 * H_kv and H_kv in {1, 2, 4, 8, 16, 32, 64};
+ * head_dim 128; 64-token blocks -- else HPC_ERR_UNSUPPORTED.
+ * The first call on a plan from hpc_decode_plan / _static allocates its
+ * partial workspace (plans from hpc_decode_plan_create already have it).
+ * Bad block ids read zeros and set HPC_DEVCHK_BAD_BLOCK; see
+ * hpc_decode_plan_status.
+ */
+hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
+                           const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                           const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                           hpc_tensor* lse, void* stream);
+
+/* hpc_decode_attn_ex -- hpc_decode_attn with an explicit softmax scale
+ * (> 0; a value <= 0 selects 1/sqrt(head_dim)). */
+hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
+                              const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                              const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                              hpc_tensor* lse, float softmax_scale, void* stream);
+
+/*
+ * hpc_decode_plan_set_timing_events -- instrumentation: while set, each
+ * hpc_decode_attn on this plan records `ev_start` just before the attention
+ * kernel, `ev_attn_done` between the attention and merge kernels, and
+ * `ev_end` after the merge kernel, all on the call's stream. Each argument is
+ * a cudaEvent_t owned by the caller, or NULL (not recorded).
+ */
+hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, void* ev_attn_done,
+                                             void* ev_end);
+
+/* hpc_device_sm_count -- streaming multiprocessors of the current device. */
+hpc_status hpc_device_sm_count(int32_t* num_sms);
+
+/* hpc_last_error -- message of the calling thread's last failure ("" if none). */
+const char* hpc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HPC_DECODE_H */

@@ -1,0 +1,737 @@
+// Split-KV paged GQA decode attention for sm_103a, and the log-sum-exp merge.
+//
+// The method ("vLLM x HPC-Ops", section "Attention Backend: Dynamic
+// Load-Balanced Scheduling"): a persistent grid whose CTAs each walk a list
+// of 64-token KV tiles chosen by the per-step planner; each CTA computes
+// split-KV attention of one query token per sequence over its tiles and
+// leaves a partial softmax state where a sequence spans several CTAs; a merge
+// pass combines the partial states. Paged 64-token blocks and the fp8_e4m3
+// cache come from section "Using HPC-Ops Backends in vLLM"; the GQA shape
+// (8 query heads per KV head, head_dim 128) from the 24-ai.news Hy3 paragraph.
+//
+// GB300 design (the pages' Hopper kernel is not described beyond the above):
+//  * One CTA per SM: 1 producer warp + NC consumer warps.
+//  * Work unit = (tile, kv head): one 64x128 K tile and one V tile, 16 KB
+//    each in BF16 (8 KB in FP8), fetched by TMA (4-D tensor map over
+//    [blocks][kv heads][64 slots][128], 128-byte swizzle, L2 evict-first)
+//    into a STAGES-deep shared-memory ring guarded by mbarriers.
+//  * Consumer warp math on the tensor cores with mma.sync m16n8k16, in the
+//    transposed orientation so no row is padded: S^T = K Q^T (M = 16 tokens,
+//    N = the 8 query heads of the group, K = head dim), online softmax in
+//    registers, then O^T = V^T P^T (M = head dim, N = 8 heads, K = tokens).
+//    P^T reaches the B-operand layout with movmatrix (no shared memory).
+//  * FP8 e4m3 tiles are widened in registers with cvt.f16x2.e4m3x2 (exact)
+//    and multiplied in f16; Q is given a power-of-two scale into f16 range;
+//    k_scale folds into the softmax scale, v_scale into the epilogue.
+//  * Every wait is bounded (globaltimer); a timeout sets an error bit and the
+//    CTA drains its own in-flight copies before leaving. No trap, no assert.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "hpc_internal.h"
+
+namespace hpc {
+
+namespace {
+
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          bar),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// lo -> bits 0..15, hi -> bits 16..31
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two e4m3 bytes (low byte -> low half) to f16x2; exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x16) {
+  uint32_t r;
+  const uint16_t h = (uint16_t)(x16 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait on an mbarrier phase. Returns false when the CTA is aborting
+// or the time limit passed (then the abort flag and the error bit are set).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* err, unsigned long long limit_ns,
+                                           bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        atomicOr(err, HPC_DEVCHK_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <bool FP8>
+struct Geom {
+  static constexpr int kTileBytes = FP8 ? 8192 : 16384;  // one 64 x 128 tile
+  static constexpr int kStageBytes = 2 * kTileBytes;     // K + V
+};
+
+constexpr int kCombineFloats = 36;  // per lane: acc[32], m[2], l[2]
+
+template <bool FP8, int STAGES, int NC, bool COMBINE>
+struct KernelCfg {
+  static constexpr int kThreads = (NC + 1) * 32;
+  static constexpr int kBarOff = STAGES * Geom<FP8>::kStageBytes;
+  static constexpr int kAbortOff = kBarOff + 2 * STAGES * 8;
+  static constexpr int kCombOff = kAbortOff + 16;
+  static constexpr int kSmemBytes =
+      1024 /* alignment slack */ + kCombOff + (COMBINE ? NC * 32 * kCombineFloats * 4 : 0);
+};
+
+// Output coordinate of accumulator element (dm, r): BF16 rows are d = 16dm+g
+// (+8); the FP8 V path permutes rows so a thread owns d = 16dm+2g (+1).
+template <bool FP8>
+__device__ __forceinline__ int acc_d(int dm, int r, int g) {
+  return FP8 ? (16 * dm + 2 * g + r) : (16 * dm + g + 8 * r);
+}
+
+// Q of one (sequence, kv head) as mma B fragments (B[k = d][n = q head]).
+template <bool FP8>
+__device__ __forceinline__ float load_q(const AttnParams& p, int b, int h, int lane,
+                                        uint32_t (&qf)[8][2]) {
+  const int g = lane >> 2, c = lane & 3;
+  const __nv_bfloat16* qrow = p.q + (int64_t)b * p.q_sb + (int64_t)(h * kGroup + g) * p.q_sh;
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c));
+      qf[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c + 8));
+    }
+    return 1.0f;
+  } else {
+    // Logical k (2c, 2c+1 | 2c+8, 2c+9) of k-step ks maps to d = 16ks + 4c + (0,1 | 2,3),
+    // matching the byte order ldmatrix gives the FP8 K tile.
+    float v[8][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c));
+      v[ks][0] = __uint_as_float(u.x << 16);
+      v[ks][1] = __uint_as_float(u.x & 0xFFFF0000u);
+      v[ks][2] = __uint_as_float(u.y << 16);
+      v[ks][3] = __uint_as_float(u.y & 0xFFFF0000u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[ks][e]));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // Power-of-two scale putting max|q| in [2^14, 2^15): f16 holds every
+    // bf16 value of that range exactly.
+    int e = 0;
+    if (amax > 0.f) {
+      const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+      e = 14 - ex;
+      e = e < -60 ? -60 : (e > 60 ? 60 : e);
+    }
+    const float sc = __uint_as_float((uint32_t)(e + 127) << 23);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = pack_f16(v[ks][0] * sc, v[ks][1] * sc);
+      qf[ks][1] = pack_f16(v[ks][2] * sc, v[ks][3] * sc);
+    }
+    return __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  }
+}
+
+// One (tile, kv head) unit: scores, online softmax update, P.V accumulate.
+template <bool FP8>
+__device__ __forceinline__ void compute_unit(uint32_t kbase, uint32_t vbase,
+                                             const uint32_t (&qf)[8][2], int valid, float sl2,
+                                             float (&m)[2], float (&l)[2], float (&acc)[8][4],
+                                             int lane) {
+  const int r8 = lane & 7;
+  const int mi = lane >> 3;
+  const int g = lane >> 2;
+  float s[4][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+
+  // ---- S^T = K Q^T
+  const uint32_t k_lane = kbase + (uint32_t)((r8 + (mi & 1) * 8) * 128);
+  if constexpr (!FP8) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t off = (uint32_t)((ks >> 2) * 8192 + ((((2 * ks) & 7) + (mi >> 1)) ^ r8) * 16);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(k_lane + mt * 2048 + off, a0, a1, a2, a3);
+        mma_bf16(s[mt], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+      const uint32_t off = (uint32_t)((((2 * kp) + (mi >> 1)) ^ r8) * 16);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(k_lane + mt * 2048 + off, r0, r1, r2, r3);
+        mma_f16(s[mt], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
+        mma_f16(s[mt], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+      }
+    }
+  }
+
+  // ---- online softmax (log2 domain); columns 2c (e=0) and 2c+1 (e=1)
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int tok = mt * 16 + g + 8 * r;
+      float x0 = s[mt][2 * r] * sl2, x1 = s[mt][2 * r + 1] * sl2;
+      if (tok >= valid) x0 = x1 = -INFINITY;
+      s[mt][2 * r] = x0;
+      s[mt][2 * r + 1] = x1;
+      mx0 = fmaxf(mx0, x0);
+      mx1 = fmaxf(mx1, x1);
+    }
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float al0 = ex2(m[0] - mn0), al1 = ex2(m[1] - mn1);
+  m[0] = mn0;
+  m[1] = mn1;
+  float ps0 = 0.f, ps1 = 0.f;
+  uint32_t pb[4][2];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    const float p0 = ex2(s[mt][0] - mn0), p1 = ex2(s[mt][1] - mn1);
+    const float p2 = ex2(s[mt][2] - mn0), p3 = ex2(s[mt][3] - mn1);
+    ps0 += p0 + p2;
+    ps1 += p1 + p3;
+    if constexpr (!FP8) {
+      pb[mt][0] = movm_trans(pack_bf16(p0, p1));
+      pb[mt][1] = movm_trans(pack_bf16(p2, p3));
+    } else {
+      pb[mt][0] = movm_trans(pack_f16(p0, p1));
+      pb[mt][1] = movm_trans(pack_f16(p2, p3));
+    }
+  }
+  l[0] = l[0] * al0 + ps0;
+  l[1] = l[1] * al1 + ps1;
+#pragma unroll
+  for (int dm = 0; dm < 8; ++dm) {
+    acc[dm][0] *= al0;
+    acc[dm][1] *= al1;
+    acc[dm][2] *= al0;
+    acc[dm][3] *= al1;
+  }
+
+  // ---- O^T += V^T P^T
+  if constexpr (!FP8) {
+    const uint32_t v_lane = vbase + (uint32_t)(((r8) + ((mi >> 1) << 3)) * 128);
+#pragma unroll
+    for (int dm = 0; dm < 8; ++dm) {
+      const uint32_t off = (uint32_t)((dm >> 2) * 8192 + ((((2 * dm) & 7) + (mi & 1)) ^ r8) * 16);
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(v_lane + kt * 2048 + off, a0, a1, a2, a3);
+        mma_bf16(acc[dm], a0, a1, a2, a3, pb[kt][0], pb[kt][1]);
+      }
+    }
+  } else {
+    const uint32_t v_lane = vbase + (uint32_t)((r8 + ((mi & 1) << 3)) * 128);
+#pragma unroll
+    for (int dp = 0; dp < 4; ++dp) {
+      const uint32_t off = (uint32_t)((((2 * dp) + (mi >> 1)) ^ r8) * 16);
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(v_lane + kt * 2048 + off, r0, r1, r2, r3);
+        // bytes {0,2} = (token 2c, 2c+1) at even d; bytes {1,3} at odd d
+        const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
+        const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
+        mma_f16(acc[2 * dp], e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1),
+                e4m3x2_to_f16x2(x1 >> 16), pb[kt][0], pb[kt][1]);
+        mma_f16(acc[2 * dp + 1], e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x2 >> 16),
+                e4m3x2_to_f16x2(x3), e4m3x2_to_f16x2(x3 >> 16), pb[kt][0], pb[kt][1]);
+      }
+    }
+  }
+}
+
+// Final output (whole sequence in this CTA) or a partial state.
+template <bool FP8>
+__device__ __forceinline__ void write_result(const AttnParams& p, bool whole, int b, int h, int seg,
+                                             const float (&m)[2], const float (&l)[2],
+                                             const float (&acc)[8][4], int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  if (whole) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = h * kGroup + 2 * c + e;
+      const float inv = l[e] > 0.f ? p.v_scale / l[e] : 0.f;
+      __nv_bfloat16* orow = p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh;
+      if constexpr (FP8) {
+#pragma unroll
+        for (int dm = 0; dm < 8; ++dm)
+          *reinterpret_cast<__nv_bfloat162*>(orow + acc_d<true>(dm, 0, g)) =
+              __floats2bfloat162_rn(acc[dm][e] * inv, acc[dm][2 + e] * inv);
+      } else {
+#pragma unroll
+        for (int dm = 0; dm < 8; ++dm) {
+          orow[acc_d<false>(dm, 0, g)] = __float2bfloat16_rn(acc[dm][e] * inv);
+          orow[acc_d<false>(dm, 1, g)] = __float2bfloat16_rn(acc[dm][2 + e] * inv);
+        }
+      }
+      if (p.lse && g == 0)
+        p.lse[(int64_t)b * p.l_sb + (int64_t)j * p.l_sh] =
+            l[e] > 0.f ? (m[e] + __log2f(l[e])) * kLn2 : -INFINITY;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = h * kGroup + 2 * c + e;
+      float* o = p.ws_o + ((int64_t)seg * p.num_q_heads + j) * kHeadDim;
+#pragma unroll
+      for (int dm = 0; dm < 8; ++dm) {
+        if constexpr (FP8) {
+          *reinterpret_cast<float2*>(o + acc_d<true>(dm, 0, g)) =
+              make_float2(acc[dm][e] * p.v_scale, acc[dm][2 + e] * p.v_scale);
+        } else {
+          o[acc_d<false>(dm, 0, g)] = acc[dm][e];
+          o[acc_d<false>(dm, 1, g)] = acc[dm][2 + e];
+        }
+      }
+      if (g == 0) {
+        p.ws_m[(int64_t)seg * p.num_q_heads + j] = m[e];
+        p.ws_l[(int64_t)seg * p.num_q_heads + j] = l[e];
+      }
+    }
+  }
+}
+
+template <bool FP8, int STAGES, int NC, bool COMBINE>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
+    attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv) {
+  using Cfg = KernelCfg<FP8, STAGES, NC, COMBINE>;
+  constexpr int kTile = Geom<FP8>::kTileBytes;
+  constexpr int kStage = Geom<FP8>::kStageBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t bar_full = smem_base + Cfg::kBarOff;
+  const uint32_t bar_empty = bar_full + STAGES * 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kAbortOff);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  int seg_begin, seg_end, h_begin, h_count;
+  if (p.static_mode) {
+    seg_begin = blockIdx.x;
+    seg_end = seg_begin + 1;
+    h_begin = blockIdx.y;
+    h_count = 1;
+  } else {
+    if ((int)blockIdx.x >= p.plan[kNumParts]) return;  // fewer parts than CTAs
+    seg_begin = p.plan[p.part_off + blockIdx.x];
+    seg_end = p.plan[p.part_off + blockIdx.x + 1];
+    h_begin = 0;
+    h_count = p.num_kv_heads;
+  }
+  const int hpass = h_count < NC ? h_count : NC;  // kv heads processed together
+  const int npass = h_count / hpass;
+  const int wph = NC / hpass;                     // consumer warps per kv head
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == NC) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = evict_first_policy();
+    uint32_t g = 0, issued = 0;
+    bool stop = false;
+    for (int seg = seg_begin; seg < seg_end; ++seg) {
+      const int4 rec = *reinterpret_cast<const int4*>(p.plan + p.seg_off + 4 * seg);
+      const int b = rec.x, tb = rec.y, n = rec.z - rec.y;
+      const int32_t* btrow = p.block_table + (int64_t)b * p.bt_sb;
+      for (int pass = 0; pass < npass; ++pass) {
+        for (int i0 = 0; i0 < n; i0 += 32) {
+          const int i = i0 + lane;
+          int blk = p.num_blocks;  // out of range: TMA fills zeros
+          if (i < n) {
+            const int t = tb + i;
+            if (t < p.max_blocks) {
+              const int v = __ldg(btrow + t);
+              if (v >= 0 && v < p.num_blocks) blk = v;
+              else atomicOr(p.err, HPC_DEVCHK_BAD_BLOCK);
+            } else {
+              atomicOr(p.err, HPC_DEVCHK_TABLE_TOO_SHORT);
+            }
+          }
+          const int cnt = n - i0 < 32 ? n - i0 : 32;
+          for (int ii = 0; ii < cnt; ++ii) {
+            const int bk = __shfl_sync(0xffffffffu, blk, ii);
+            for (int hl = 0; hl < hpass; ++hl, ++g) {
+              if (lane != 0 || stop) continue;
+              const int h = h_begin + pass * hpass + hl;
+              const uint32_t slot = g % STAGES;
+              const uint32_t par = ((g / STAGES) & 1u) ^ 1u;
+              if (!wait_phase(bar_empty + 8 * slot, par, abort_flag, p.err, p.timeout_ns)) {
+                stop = true;
+                continue;
+              }
+              const uint32_t fb = bar_full + 8 * slot;
+              const uint32_t dk = smem_base + slot * kStage;
+              const uint32_t dv = dk + kTile;
+              const int c1 = p.kv_swap ? h : 0, c2 = p.kv_swap ? 0 : h;
+              mbar_arrive_expect_tx(fb, kStage);
+              if constexpr (FP8) {
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
+              } else {
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dk + 8192, &tmk, fb, 64, c1, c2, bk, policy);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dv + 8192, &tmv, fb, 64, c1, c2, bk, policy);
+              }
+              issued = g + 1;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0 && stop) {
+      // Aborting: wait (bounded) for this CTA's own copies still in flight.
+      for (uint32_t u = issued > (uint32_t)STAGES ? issued - STAGES : 0; u < issued; ++u)
+        wait_phase(bar_full + 8 * (u % STAGES), (u / STAGES) & 1u, abort_flag, p.err,
+                   1000000000ull, false);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  float* comb = reinterpret_cast<float*>(smem + Cfg::kCombOff);
+  const int hl = warp % hpass;      // kv head (within the pass) of this warp
+  const int tphase = warp / hpass;  // this warp takes tiles i = tphase (mod wph)
+  const int c = lane & 3;
+  uint32_t gbase = 0;
+  bool dead = false;
+  for (int seg = seg_begin; seg < seg_end; ++seg) {
+    const int4 rec = *reinterpret_cast<const int4*>(p.plan + p.seg_off + 4 * seg);
+    const int b = rec.x, tb = rec.y, n = rec.z - rec.y;
+    const bool whole = (rec.w & HPC_SEG_WHOLE) != 0;
+    const int len = p.seq_lens[b];
+    if (warp == 0 && lane == 0) {
+      const int n_plan = p.plan[p.cu_off + b + 1] - p.plan[p.cu_off + b];
+      const int n_dev = len > 0 ? (len + kBlockTokens - 1) / kBlockTokens : 0;
+      if (n_plan != n_dev) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
+    }
+    for (int pass = 0; pass < npass; ++pass) {
+      const int h = h_begin + pass * hpass + hl;
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      float acc[8][4];
+#pragma unroll
+      for (int dm = 0; dm < 8; ++dm) acc[dm][0] = acc[dm][1] = acc[dm][2] = acc[dm][3] = 0.f;
+      if (tphase < n) {
+        uint32_t qf[8][2];
+        const float qinv = load_q<FP8>(p, b, h, lane, qf);
+        const float sl2 = p.score_scale_log2 * qinv;
+        for (int i = tphase; i < n; i += wph) {
+          const uint32_t gu = gbase + (uint32_t)(i * hpass + hl);
+          const uint32_t slot = gu % STAGES;
+          if (dead) continue;
+          const bool ok = wait_phase(bar_full + 8 * slot, (gu / STAGES) & 1u, abort_flag, p.err,
+                                     p.timeout_ns);
+          if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform decision
+            dead = true;
+            continue;
+          }
+          const int valid = len - (tb + i) * kBlockTokens;
+          if (valid > 0) {
+            const uint32_t kb = smem_base + slot * kStage;
+            compute_unit<FP8>(kb, kb + kTile, qf, valid, sl2, m, l, acc, lane);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+        }
+      }
+      gbase += (uint32_t)(n * hpass);
+      // reduce the row sums over the 8 lanes sharing a column pair
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
+      }
+      if (!COMBINE || wph == 1) {
+        if (!dead) write_result<FP8>(p, whole, b, h, seg, m, l, acc, lane);
+      } else {
+        if (tphase > 0) {
+          float* cw = comb + (warp * 32 + lane) * kCombineFloats;
+#pragma unroll
+          for (int dm = 0; dm < 8; ++dm)
+            *reinterpret_cast<float4*>(cw + 4 * dm) =
+                make_float4(acc[dm][0], acc[dm][1], acc[dm][2], acc[dm][3]);
+          *reinterpret_cast<float4*>(cw + 32) = make_float4(m[0], m[1], l[0], l[1]);
+        }
+        named_bar_sync(1, NC * 32);
+        if (tphase == 0) {
+          float M0 = m[0], M1 = m[1];
+          for (int k = 1; k < wph; ++k) {
+            const float4 ml =
+                *reinterpret_cast<const float4*>(comb + ((warp + k * hpass) * 32 + lane) *
+                                                            kCombineFloats + 32);
+            M0 = fmaxf(M0, ml.x);
+            M1 = fmaxf(M1, ml.y);
+          }
+          const float f0 = m[0] == -INFINITY ? 0.f : ex2(m[0] - M0);
+          const float f1 = m[1] == -INFINITY ? 0.f : ex2(m[1] - M1);
+          l[0] *= f0;
+          l[1] *= f1;
+#pragma unroll
+          for (int dm = 0; dm < 8; ++dm) {
+            acc[dm][0] *= f0;
+            acc[dm][1] *= f1;
+            acc[dm][2] *= f0;
+            acc[dm][3] *= f1;
+          }
+          for (int k = 1; k < wph; ++k) {
+            const float* cw = comb + ((warp + k * hpass) * 32 + lane) * kCombineFloats;
+            const float4 ml = *reinterpret_cast<const float4*>(cw + 32);
+            const float k0 = ml.x == -INFINITY ? 0.f : ex2(ml.x - M0);
+            const float k1 = ml.y == -INFINITY ? 0.f : ex2(ml.y - M1);
+            l[0] += ml.z * k0;
+            l[1] += ml.w * k1;
+#pragma unroll
+            for (int dm = 0; dm < 8; ++dm) {
+              const float4 a = *reinterpret_cast<const float4*>(cw + 4 * dm);
+              acc[dm][0] += a.x * k0;
+              acc[dm][1] += a.y * k1;
+              acc[dm][2] += a.z * k0;
+              acc[dm][3] += a.w * k1;
+            }
+          }
+          m[0] = M0;
+          m[1] = M1;
+          if (!*abort_flag) write_result<FP8>(p, whole, b, h, seg, m, l, acc, lane);
+        }
+        named_bar_sync(1, NC * 32);
+      }
+    }
+  }
+  (void)c;
+}
+
+// ------------------------------------------------------------------ merge
+constexpr int kMergeThreads = 256;  // 8 query heads x 32 lanes x 4 dims
+
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
+  const int b = blockIdx.x, hk = blockIdx.y;
+  const int s0 = p.plan[p.seq_off + b], s1 = p.plan[p.seq_off + b + 1];
+  const int ns = s1 - s0;
+  if (ns == 1) return;  // written by the attention kernel
+  const int j = hk * kGroup + (threadIdx.x >> 5);
+  const int d0 = (threadIdx.x & 31) * 4;
+  __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh + d0;
+  float* lse = p.lse ? p.lse + (int64_t)b * p.l_sb + (int64_t)j * p.l_sh : nullptr;
+  float M = -INFINITY;
+  for (int s = s0; s < s1; ++s) M = fmaxf(M, p.ws_m[(int64_t)s * p.num_q_heads + j]);
+  if (ns == 0 || M == -INFINITY) {
+    // empty sequence: out = 0, lse = -inf
+    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
+    if (lse && (threadIdx.x & 31) == 0) *lse = -INFINITY;
+    return;
+  }
+  float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  constexpr int U = 8;
+  int s = s0;
+  for (; s + U <= s1; s += U) {
+    float mm[U], ll[U];
+    float4 oo[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t r = (int64_t)(s + u) * p.num_q_heads + j;
+      mm[u] = p.ws_m[r];
+      ll[u] = p.ws_l[r];
+      oo[u] = *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + d0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float w = ex2(mm[u] - M);
+      l += ll[u] * w;
+      a0 += oo[u].x * w;
+      a1 += oo[u].y * w;
+      a2 += oo[u].z * w;
+      a3 += oo[u].w * w;
+    }
+  }
+  for (; s < s1; ++s) {
+    const int64_t r = (int64_t)s * p.num_q_heads + j;
+    const float w = ex2(p.ws_m[r] - M);
+    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + d0);
+    l += p.ws_l[r] * w;
+    a0 += v.x * w;
+    a1 += v.y * w;
+    a2 += v.z * w;
+    a3 += v.w * w;
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 * inv, a1 * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(a2 * inv, a3 * inv);
+  *reinterpret_cast<uint2*>(o) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  if (lse && (threadIdx.x & 31) == 0) *lse = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
+}
+
+template <bool FP8, int STAGES, int NC, bool COMBINE>
+cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx,
+                       int gy, cudaStream_t stream) {
+  using Cfg = KernelCfg<FP8, STAGES, NC, COMBINE>;
+  auto kern = attn_kernel<FP8, STAGES, NC, COMBINE>;
+  static bool configured = false;  // per instantiation; attribute is per device function
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<dim3(gx, gy), Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             bool fp8, int gx, int gy, cudaStream_t stream) {
+  const int hc = p.static_mode ? 1 : p.num_kv_heads;
+  const bool combine = hc < 8;
+  if (fp8) {
+    return combine ? launch_cfg<true, 10, 8, true>(p, tk, tv, gx, gy, stream)
+                   : launch_cfg<true, 12, 8, false>(p, tk, tv, gx, gy, stream);
+  }
+  return combine ? launch_cfg<false, 5, 8, true>(p, tk, tv, gx, gy, stream)
+                 : launch_cfg<false, 6, 8, false>(p, tk, tv, gx, gy, stream);
+}
+
+cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_t stream) {
+  if (p.num_seqs == 0) return cudaSuccess;
+  merge_kernel<<<dim3(p.num_seqs, num_kv_heads), kMergeThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace hpc

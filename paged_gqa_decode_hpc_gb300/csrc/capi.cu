@@ -1,0 +1,582 @@
+// C ABI of libhpc_decode.so: argument checks, plan objects, TMA descriptors
+// and launches. See include/hpc_decode.h for the contract of every call.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "hpc_internal.h"
+
+namespace hpc {
+
+namespace {
+thread_local std::string g_last_error;
+
+hpc_status fail(hpc_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+#define HPC_CUDA_TRY(expr)                                                                  \
+  do {                                                                                      \
+    cudaError_t e__ = (expr);                                                               \
+    if (e__ != cudaSuccess) {                                                               \
+      return fail(e__ == cudaErrorMemoryAllocation ? HPC_ERR_OOM : HPC_ERR_CUDA,            \
+                  std::string(#expr) + ": " + cudaGetErrorString(e__));                     \
+    }                                                                                       \
+  } while (0)
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* s = std::getenv("HPC_DECODE_WAIT_LIMIT_MS");
+    long long ms = s ? std::atoll(s) : 2000;
+    if (ms < 0) ms = 2000;
+    return (unsigned long long)ms * 1000000ull;
+  }();
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+void free_plan(hpc_plan_s* pl) {
+  if (!pl) return;
+  if (pl->d_words) cudaFree(pl->d_words);
+  if (pl->d_err) cudaFree(pl->d_err);
+  if (pl->d_ws) cudaFree(pl->d_ws);
+  if (pl->h_pinned) cudaFreeHost(pl->h_pinned);
+  if (pl->copy_done) cudaEventDestroy(pl->copy_done);
+  delete pl;
+}
+
+// Allocate the plan buffer + error word for layout L on the current device.
+hpc_status alloc_plan_buffers(hpc_plan_s* pl) {
+  HPC_CUDA_TRY(cudaGetDevice(&pl->device));
+  HPC_CUDA_TRY(cudaMalloc(&pl->d_words, (size_t)pl->layout.words() * sizeof(int32_t)));
+  HPC_CUDA_TRY(cudaMalloc(&pl->d_err, sizeof(int32_t)));
+  HPC_CUDA_TRY(cudaMemset(pl->d_err, 0, sizeof(int32_t)));
+  return HPC_OK;
+}
+
+hpc_status ensure_workspace(hpc_plan_s* pl, int64_t num_q_heads, bool may_allocate) {
+  if (pl->d_ws && pl->ws_heads >= num_q_heads) return HPC_OK;
+  if (!may_allocate)
+    return fail(HPC_ERR_INVALID_ARG,
+                "plan workspace was sized for fewer query heads; create the plan with "
+                "num_q_heads >= " + std::to_string(num_q_heads));
+  if (pl->d_ws) {
+    HPC_CUDA_TRY(cudaDeviceSynchronize());
+    cudaFree(pl->d_ws);
+    pl->d_ws = nullptr;
+  }
+  const size_t floats = (size_t)std::max<int64_t>(pl->layout.cap_segs, 1) * num_q_heads *
+                        (kHeadDim + 2);
+  HPC_CUDA_TRY(cudaMalloc(&pl->d_ws, floats * sizeof(float)));
+  pl->ws_heads = num_q_heads;
+  return HPC_OK;
+}
+
+int elt_bytes(int32_t dt) {
+  switch (dt) {
+    case HPC_BF16: return 2;
+    case HPC_FP8_E4M3: return 1;
+    case HPC_F32: case HPC_I32: return 4;
+    default: return 0;
+  }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+hpc_status check_tensor(const hpc_tensor* t, const char* name, int ndim, bool nullable = false) {
+  if (!t || !t->data) {
+    if (nullable && (!t || !t->data)) return HPC_OK;
+    return fail(HPC_ERR_INVALID_ARG, std::string(name) + " is null");
+  }
+  if (t->ndim != ndim)
+    return fail(HPC_ERR_INVALID_ARG, std::string(name) + " must have " + std::to_string(ndim) +
+                                         " dimensions");
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0)
+      return fail(HPC_ERR_INVALID_ARG, std::string(name) + " has a negative shape or stride");
+  if (elt_bytes(t->dtype) == 0) return fail(HPC_ERR_INVALID_ARG, std::string(name) + ": bad dtype");
+  return HPC_OK;
+}
+
+// 4-D TMA descriptor over a [blocks][kv heads][64][128] cache (any strides
+// that are multiples of 16 bytes). The two middle dimensions are ordered by
+// stride so that either cache layout maps onto a monotone tensor.
+hpc_status make_kv_map(const hpc_tensor* t, bool fp8, bool swap, CUtensorMap* map) {
+  auto enc = encode_fn();
+  if (!enc) return fail(HPC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const int64_t e = fp8 ? 1 : 2;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  dims[0] = kHeadDim;
+  box[0] = fp8 ? 128 : 64;
+  if (!swap) {
+    dims[1] = kBlockTokens; dims[2] = (cuuint64_t)t->shape[1];
+    strides[0] = t->stride[2] * e; strides[1] = t->stride[1] * e;
+    box[1] = kBlockTokens; box[2] = 1;
+  } else {
+    dims[1] = (cuuint64_t)t->shape[1]; dims[2] = kBlockTokens;
+    strides[0] = t->stride[1] * e; strides[1] = t->stride[2] * e;
+    box[1] = 1; box[2] = kBlockTokens;
+  }
+  dims[3] = (cuuint64_t)t->shape[0];
+  strides[2] = t->stride[0] * e;
+  box[3] = 1;
+  CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   t->data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(HPC_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the KV cache (error " +
+                                         std::to_string((int)r) + ")");
+  return HPC_OK;
+}
+
+// Copy a capacity-layout word array into the canonical export layout.
+hpc_status write_canonical(const int32_t* w, const PlanLayout& L, int32_t* buf, int64_t cap,
+                           int64_t* len) {
+  const int32_t B = w[kNumSeqs], P = w[kNumParts], S = w[kNumSegs];
+  if (w[kMagic] != kPlanMagic || B < 0 || B > L.cap_seqs || P < 0 || P > L.cap_parts || S < 0 ||
+      S > L.cap_segs)
+    return fail(HPC_ERR_DEVICE_CHECK, "plan buffer is inconsistent");
+  const int64_t n = kHeaderWords + (P + 1) + (B + 1) + 4LL * S;
+  *len = n;
+  if (cap == 0 && !buf) return HPC_OK;
+  if (!buf || cap < n) return fail(HPC_ERR_INVALID_ARG, "export buffer too small");
+  int64_t o = 0;
+  for (int i = 0; i < kHeaderWords; ++i) buf[o++] = w[i];
+  for (int i = 0; i <= P; ++i) buf[o++] = w[L.part_off() + i];
+  for (int i = 0; i <= B; ++i) buf[o++] = w[L.seq_off() + i];
+  for (int64_t i = 0; i < 4LL * S; ++i) buf[o++] = w[L.seg_off() + i];
+  return HPC_OK;
+}
+
+hpc_status new_host_plan(const int32_t* words, const PlanLayout& L, int32_t kind,
+                         int32_t num_sms, int32_t num_seqs, int32_t parts, int32_t segs,
+                         int32_t kv_heads, hpc_plan_t* out) {
+  hpc_plan_s* pl = new (std::nothrow) hpc_plan_s();
+  if (!pl) return fail(HPC_ERR_OOM, "host allocation failed");
+  pl->kind = kind;
+  pl->layout = L;
+  pl->num_sms = num_sms;
+  pl->max_seqs = num_seqs;
+  pl->num_seqs = num_seqs;
+  pl->host_num_parts = parts;
+  pl->host_num_segs = segs;
+  pl->static_kv_heads = kv_heads;
+  hpc_status st = alloc_plan_buffers(pl);
+  if (st == HPC_OK) {
+    cudaError_t e = cudaMemcpy(pl->d_words, words, (size_t)L.words() * sizeof(int32_t),
+                               cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) st = fail(HPC_ERR_CUDA, std::string("plan upload: ") +
+                                                      cudaGetErrorString(e));
+  }
+  if (st != HPC_OK) {
+    free_plan(pl);
+    return st;
+  }
+  *out = pl;
+  return HPC_OK;
+}
+
+}  // namespace
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+}  // namespace hpc
+
+using namespace hpc;
+
+extern "C" {
+
+const char* hpc_last_error(void) { return g_last_error.c_str(); }
+
+hpc_status hpc_device_sm_count(int32_t* num_sms) {
+  if (!num_sms) return fail(HPC_ERR_INVALID_ARG, "num_sms is null");
+  int dev = 0, n = 0;
+  HPC_CUDA_TRY(cudaGetDevice(&dev));
+  HPC_CUDA_TRY(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+  *num_sms = n;
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                           hpc_plan_t* plan_out) {
+  if (!plan_out) return fail(HPC_ERR_INVALID_ARG, "plan_out is null");
+  *plan_out = nullptr;
+  if (num_seqs < 0 || (num_seqs > 0 && !seq_lens))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens is null or num_seqs < 0");
+  if (num_sms <= 0) return fail(HPC_ERR_INVALID_ARG, "num_sms must be positive");
+  int64_t T = 0;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    if (seq_lens[b] < 0)
+      return fail(HPC_ERR_INVALID_ARG, "negative sequence length at index " + std::to_string(b));
+    T += (seq_lens[b] + (int64_t)kBlockTokens - 1) / kBlockTokens;
+  }
+  PlanLayout L;
+  L.cap_seqs = num_seqs;
+  L.cap_parts = (int32_t)std::min<int64_t>(num_sms, T);
+  L.cap_segs = (int32_t)dynamic_max_segs(num_seqs, L.cap_parts);
+  std::vector<int32_t> w((size_t)L.words(), 0);
+  std::string err;
+  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err);
+  if (st != HPC_OK) return fail(st, err);
+  return new_host_plan(w.data(), L, HPC_PLAN_DYNAMIC, num_sms, num_seqs, w[kNumParts],
+                       w[kNumSegs], 0, plan_out);
+}
+
+hpc_status hpc_decode_plan_static(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                  int32_t num_kv_heads, int32_t num_splits,
+                                  hpc_plan_t* plan_out) {
+  if (!plan_out) return fail(HPC_ERR_INVALID_ARG, "plan_out is null");
+  *plan_out = nullptr;
+  int32_t* w = nullptr;
+  PlanLayout L;
+  std::string err;
+  hpc_status st =
+      plan_static_host(seq_lens, num_seqs, num_sms, num_kv_heads, num_splits, &w, &L, &err);
+  if (st != HPC_OK) return fail(st, err);
+  st = new_host_plan(w, L, HPC_PLAN_STATIC, num_sms, num_seqs, w[kNumParts], w[kNumSegs],
+                     num_kv_heads, plan_out);
+  free(w);
+  return st;
+}
+
+hpc_status hpc_decode_plan_create(int32_t max_seqs, int32_t num_sms, int32_t num_q_heads,
+                                  hpc_plan_t* plan_out) {
+  if (!plan_out) return fail(HPC_ERR_INVALID_ARG, "plan_out is null");
+  *plan_out = nullptr;
+  if (max_seqs < 0 || num_sms <= 0 || num_q_heads <= 0)
+    return fail(HPC_ERR_INVALID_ARG, "max_seqs >= 0, num_sms > 0 and num_q_heads > 0 required");
+  hpc_plan_s* pl = new (std::nothrow) hpc_plan_s();
+  if (!pl) return fail(HPC_ERR_OOM, "host allocation failed");
+  pl->kind = HPC_PLAN_DYNAMIC;
+  pl->layout.cap_seqs = max_seqs;
+  pl->layout.cap_parts = num_sms;
+  pl->layout.cap_segs = (int32_t)dynamic_max_segs(max_seqs, num_sms);
+  pl->num_sms = num_sms;
+  pl->max_seqs = max_seqs;
+  pl->num_seqs = 0;
+  pl->host_num_parts = 0;
+  pl->host_num_segs = 0;
+  auto cleanup = [&](hpc_status st) {
+    free_plan(pl);
+    return st;
+  };
+  hpc_status st = alloc_plan_buffers(pl);
+  if (st != HPC_OK) return cleanup(st);
+  st = ensure_workspace(pl, num_q_heads, true);
+  if (st != HPC_OK) return cleanup(st);
+  const size_t bytes = (size_t)pl->layout.words() * sizeof(int32_t);
+  if (cudaMallocHost(&pl->h_pinned, bytes) != cudaSuccess ||
+      cudaEventCreateWithFlags(&pl->copy_done, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(fail(HPC_ERR_OOM, "pinned host allocation failed"));
+  // an empty step: zero sequences
+  std::memset(pl->h_pinned, 0, bytes);
+  std::string err;
+  st = plan_dynamic_host(nullptr, 0, num_sms, pl->h_pinned, pl->layout, &err);
+  if (st != HPC_OK) return cleanup(fail(st, err));
+  if (cudaMemcpy(pl->d_words, pl->h_pinned, bytes, cudaMemcpyHostToDevice) != cudaSuccess)
+    return cleanup(fail(HPC_ERR_CUDA, "plan upload failed"));
+  *plan_out = pl;
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_plan_device(const int32_t* seq_lens_dev, int32_t num_seqs, int32_t num_sms,
+                                  hpc_plan_t plan, void* stream) {
+  if (!plan || plan->kind != HPC_PLAN_DYNAMIC || !plan->h_pinned)
+    return fail(HPC_ERR_INVALID_ARG, "plan must come from hpc_decode_plan_create");
+  if (num_seqs < 0 || (num_seqs > 0 && !seq_lens_dev))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens_dev is null or num_seqs < 0");
+  if (num_seqs > plan->layout.cap_seqs)
+    return fail(HPC_ERR_INVALID_ARG, "num_seqs exceeds the plan's max_seqs");
+  if (num_sms <= 0 || num_sms > plan->layout.cap_parts)
+    return fail(HPC_ERR_INVALID_ARG, "num_sms must be in [1, plan num_sms]");
+  cudaError_t e = launch_plan_device(seq_lens_dev, num_seqs, num_sms, plan->d_words, plan->layout,
+                                     plan->d_err, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(HPC_ERR_CUDA, std::string("device planner launch: ") + cudaGetErrorString(e));
+  plan->num_seqs = num_seqs;
+  plan->num_sms = num_sms;
+  plan->host_num_parts = -1;
+  plan->host_num_segs = -1;
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_plan_update(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                  hpc_plan_t plan, void* stream) {
+  if (!plan || plan->kind != HPC_PLAN_DYNAMIC || !plan->h_pinned)
+    return fail(HPC_ERR_INVALID_ARG, "plan must come from hpc_decode_plan_create");
+  if (num_sms <= 0 || num_sms > plan->layout.cap_parts)
+    return fail(HPC_ERR_INVALID_ARG, "num_sms must be in [1, plan num_sms]");
+  // the staging buffer may still feed the previous upload
+  HPC_CUDA_TRY(cudaEventSynchronize(plan->copy_done));
+  std::string err;
+  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, plan->h_pinned, plan->layout,
+                                    &err);
+  if (st != HPC_OK) return fail(st, err);
+  HPC_CUDA_TRY(cudaMemcpyAsync(plan->d_words, plan->h_pinned,
+                               (size_t)plan->layout.words() * sizeof(int32_t),
+                               cudaMemcpyHostToDevice, (cudaStream_t)stream));
+  HPC_CUDA_TRY(cudaEventRecord(plan->copy_done, (cudaStream_t)stream));
+  plan->num_seqs = num_seqs;
+  plan->num_sms = num_sms;
+  plan->host_num_parts = plan->h_pinned[kNumParts];
+  plan->host_num_segs = plan->h_pinned[kNumSegs];
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, int64_t* len) {
+  if (!plan || !len) return fail(HPC_ERR_INVALID_ARG, "plan or len is null");
+  const PlanLayout& L = plan->layout;
+  std::vector<int32_t> w((size_t)L.words());
+  HPC_CUDA_TRY(cudaDeviceSynchronize());
+  HPC_CUDA_TRY(cudaMemcpy(w.data(), plan->d_words, w.size() * sizeof(int32_t),
+                          cudaMemcpyDeviceToHost));
+  return write_canonical(w.data(), L, buf, cap, len);
+}
+
+hpc_status hpc_decode_plan_compute(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                   int32_t* buf, int64_t cap, int64_t* len) {
+  if (!len) return fail(HPC_ERR_INVALID_ARG, "len is null");
+  if (num_seqs < 0 || (num_seqs > 0 && !seq_lens))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens is null or num_seqs < 0");
+  if (num_sms <= 0) return fail(HPC_ERR_INVALID_ARG, "num_sms must be positive");
+  PlanLayout L;
+  L.cap_seqs = num_seqs;
+  L.cap_parts = num_sms;
+  L.cap_segs = (int32_t)dynamic_max_segs(num_seqs, num_sms);
+  std::vector<int32_t> w((size_t)L.words(), 0);
+  std::string err;
+  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err);
+  if (st != HPC_OK) return fail(st, err);
+  return write_canonical(w.data(), L, buf, cap, len);
+}
+
+hpc_status hpc_decode_plan_static_compute(const int32_t* seq_lens, int32_t num_seqs,
+                                          int32_t num_sms, int32_t num_kv_heads,
+                                          int32_t num_splits, int32_t* buf, int64_t cap,
+                                          int64_t* len) {
+  if (!len) return fail(HPC_ERR_INVALID_ARG, "len is null");
+  int32_t* w = nullptr;
+  PlanLayout L;
+  std::string err;
+  hpc_status st =
+      plan_static_host(seq_lens, num_seqs, num_sms, num_kv_heads, num_splits, &w, &L, &err);
+  if (st != HPC_OK) return fail(st, err);
+  st = write_canonical(w, L, buf, cap, len);
+  free(w);
+  return st;
+}
+
+hpc_status hpc_decode_plan_status(hpc_plan_t plan, int32_t* device_error) {
+  if (!plan || !device_error) return fail(HPC_ERR_INVALID_ARG, "plan or device_error is null");
+  HPC_CUDA_TRY(cudaDeviceSynchronize());
+  int32_t v = 0;
+  HPC_CUDA_TRY(cudaMemcpy(&v, plan->d_err, sizeof v, cudaMemcpyDeviceToHost));
+  HPC_CUDA_TRY(cudaMemset(plan->d_err, 0, sizeof v));
+  *device_error = v;
+  if (v != 0)
+    return fail(HPC_ERR_DEVICE_CHECK, "device check fired (bits " + std::to_string(v) + ")");
+  return HPC_OK;
+}
+
+void hpc_decode_plan_destroy(hpc_plan_t plan) {
+  if (!plan) return;
+  cudaDeviceSynchronize();
+  free_plan(plan);
+}
+
+hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
+                              const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                              const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                              hpc_tensor* lse, float softmax_scale, void* stream) {
+  hpc_status st;
+  if ((st = check_tensor(q, "q", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
+  if ((st = check_tensor(v_cache, "v_cache", 4)) != HPC_OK) return st;
+  if ((st = check_tensor(block_table, "block_table", 2)) != HPC_OK) return st;
+  if ((st = check_tensor(seq_lens, "seq_lens", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(out, "out", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(lse, "lse", 2, true)) != HPC_OK) return st;
+  if (!plan) return fail(HPC_ERR_INVALID_ARG, "plan is null");
+  const bool has_lse = lse && lse->data;
+
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t NB = k_cache->shape[0], Hkv = k_cache->shape[1];
+  if (q->dtype != HPC_BF16) return fail(HPC_ERR_INVALID_ARG, "q must be bf16");
+  if (out->dtype != HPC_BF16) return fail(HPC_ERR_INVALID_ARG, "out must be bf16");
+  if (k_cache->dtype != v_cache->dtype ||
+      (k_cache->dtype != HPC_BF16 && k_cache->dtype != HPC_FP8_E4M3))
+    return fail(HPC_ERR_INVALID_ARG, "k_cache/v_cache must both be bf16 or both fp8_e4m3");
+  const bool fp8 = k_cache->dtype == HPC_FP8_E4M3;
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i] || k_cache->stride[i] != v_cache->stride[i])
+      return fail(HPC_ERR_INVALID_ARG, "k_cache and v_cache must have the same shape and strides");
+  if (D != kHeadDim || k_cache->shape[3] != kHeadDim)
+    return fail(HPC_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (k_cache->shape[2] != kBlockTokens)
+    return fail(HPC_ERR_UNSUPPORTED, "KV blocks must hold 64 tokens");
+  if (Hkv <= 0 || Hq != kGroup * Hkv)
+    return fail(HPC_ERR_UNSUPPORTED, "num_q_heads must be 8 * num_kv_heads");
+  if (!(Hkv == 1 || Hkv == 2 || Hkv == 4 || (Hkv % 8 == 0 && Hkv <= 64)))
+    return fail(HPC_ERR_UNSUPPORTED, "num_kv_heads must be 1, 2, 4, 8, 16, 32 or 64");
+  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(HPC_ERR_INVALID_ARG, "out must have q's shape");
+  if (has_lse && (lse->dtype != HPC_F32 || lse->shape[0] != B || lse->shape[1] != Hq))
+    return fail(HPC_ERR_INVALID_ARG, "lse must be f32 [B][H_q]");
+  if (block_table->dtype != HPC_I32 || block_table->shape[0] != B || block_table->stride[1] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "block_table must be int32 [B][max_blocks], row-contiguous");
+  if (seq_lens->dtype != HPC_I32 || seq_lens->shape[0] != B || (B > 1 && seq_lens->stride[0] != 1))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
+  if (q->stride[2] != 1 || out->stride[2] != 1 || k_cache->stride[3] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "innermost stride of q, out and the caches must be 1");
+  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+      !aligned(q->data, 16) || !aligned(out->data, 16))
+    return fail(HPC_ERR_INVALID_ARG, "q/out must be 16-byte aligned with strides of 8 elements");
+  const int64_t e = fp8 ? 1 : 2;
+  for (int i = 0; i < 3; ++i)
+    if ((k_cache->stride[i] * e) % 16)
+      return fail(HPC_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+  if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
+    return fail(HPC_ERR_INVALID_ARG, "cache base addresses must be 16-byte aligned");
+  // slot/head strides: either [.., H_kv, 64, 128] or [.., 64, H_kv, 128], non-overlapping
+  const int64_t s_head = k_cache->stride[1], s_slot = k_cache->stride[2],
+                s_blk = k_cache->stride[0];
+  bool swap;
+  if (s_slot >= kHeadDim && s_head >= kBlockTokens * s_slot && s_blk >= Hkv * s_head)
+    swap = false;
+  else if (s_head >= kHeadDim && s_slot >= Hkv * s_head && s_blk >= kBlockTokens * s_slot)
+    swap = true;
+  else
+    return fail(HPC_ERR_UNSUPPORTED, "cache strides must describe a [blocks][kv heads][64][128] "
+                                     "or [blocks][64][kv heads][128] layout");
+  if (plan->num_seqs != B)
+    return fail(HPC_ERR_INVALID_ARG, "plan was built for " + std::to_string(plan->num_seqs) +
+                                         " sequences, q has " + std::to_string(B));
+  if (plan->kind == HPC_PLAN_STATIC && plan->static_kv_heads != Hkv)
+    return fail(HPC_ERR_INVALID_ARG, "static plan was built for another number of kv heads");
+  if (fp8 && (!std::isfinite(k_cache->scale) || !std::isfinite(v_cache->scale)))
+    return fail(HPC_ERR_INVALID_ARG, "FP8 scales must be finite");
+  if (B == 0) return HPC_OK;
+  if (B > INT32_MAX || block_table->shape[1] > INT32_MAX || NB > INT32_MAX)
+    return fail(HPC_ERR_INVALID_ARG, "sizes exceed int32");
+
+  // grid
+  int gx, gy = 1;
+  if (plan->kind == HPC_PLAN_STATIC) {
+    gx = plan->host_num_segs;
+    gy = (int)Hkv;
+  } else {
+    gx = plan->host_num_parts >= 0 ? plan->host_num_parts : plan->num_sms;
+  }
+  st = ensure_workspace(plan, Hq, plan->h_pinned == nullptr);
+  if (st != HPC_OK) return st;
+
+  const PlanLayout& L = plan->layout;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (gx > 0) {
+    if (NB == 0) return fail(HPC_ERR_INVALID_ARG, "k_cache has no blocks");
+    CUtensorMap tk, tv;
+    if ((st = make_kv_map(k_cache, fp8, swap, &tk)) != HPC_OK) return st;
+    if ((st = make_kv_map(v_cache, fp8, swap, &tv)) != HPC_OK) return st;
+    AttnParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = (const __nv_bfloat16*)q->data;
+    p.q_sb = q->stride[0];
+    p.q_sh = q->stride[1];
+    p.out = (__nv_bfloat16*)out->data;
+    p.o_sb = out->stride[0];
+    p.o_sh = out->stride[1];
+    p.lse = has_lse ? (float*)lse->data : nullptr;
+    p.l_sb = has_lse ? lse->stride[0] : 0;
+    p.l_sh = has_lse ? lse->stride[1] : 0;
+    p.block_table = (const int32_t*)block_table->data;
+    p.bt_sb = block_table->stride[0];
+    p.max_blocks = (int32_t)block_table->shape[1];
+    p.seq_lens = (const int32_t*)seq_lens->data;
+    p.plan = plan->d_words;
+    p.seq_off = (int32_t)L.seq_off();
+    p.seg_off = (int32_t)L.seg_off();
+    p.part_off = (int32_t)L.part_off();
+    p.cu_off = (int32_t)L.cu_off();
+    p.num_seqs = (int32_t)B;
+    p.num_q_heads = (int32_t)Hq;
+    p.num_kv_heads = (int32_t)Hkv;
+    p.num_blocks = (int32_t)NB;
+    p.static_mode = plan->kind == HPC_PLAN_STATIC;
+    p.kv_swap = swap;
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+    p.score_scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_cache->scale : 1.0f);
+    p.v_scale = fp8 ? v_cache->scale : 1.0f;
+    const int64_t cs = std::max<int64_t>(L.cap_segs, 1);
+    p.ws_o = plan->d_ws;
+    p.ws_m = plan->d_ws + cs * Hq * kHeadDim;
+    p.ws_l = p.ws_m + cs * Hq;
+    p.err = plan->d_err;
+    p.timeout_ns = wait_limit_ns();
+    if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
+    cudaError_t ce = launch_attention(p, tk, tv, fp8, gx, gy, s);
+    if (ce != cudaSuccess)
+      return fail(HPC_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(ce));
+  }
+  if (plan->ev_mid) HPC_CUDA_TRY(cudaEventRecord(plan->ev_mid, s));
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof mp);
+  mp.out = (__nv_bfloat16*)out->data;
+  mp.o_sb = out->stride[0];
+  mp.o_sh = out->stride[1];
+  mp.lse = has_lse ? (float*)lse->data : nullptr;
+  mp.l_sb = has_lse ? lse->stride[0] : 0;
+  mp.l_sh = has_lse ? lse->stride[1] : 0;
+  mp.plan = plan->d_words;
+  mp.seq_off = (int32_t)L.seq_off();
+  mp.seg_off = (int32_t)L.seg_off();
+  mp.num_seqs = (int32_t)B;
+  mp.num_q_heads = (int32_t)Hq;
+  const int64_t cs = std::max<int64_t>(L.cap_segs, 1);
+  mp.ws_o = plan->d_ws;
+  mp.ws_m = plan->d_ws + cs * Hq * kHeadDim;
+  mp.ws_l = mp.ws_m + cs * Hq;
+  cudaError_t ce = launch_merge(mp, (int32_t)Hkv, s);
+  if (ce != cudaSuccess)
+    return fail(HPC_ERR_CUDA, std::string("merge launch: ") + cudaGetErrorString(ce));
+  if (plan->ev_end) HPC_CUDA_TRY(cudaEventRecord(plan->ev_end, s));
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, void* ev_attn_done,
+                                             void* ev_end) {
+  if (!plan) return fail(HPC_ERR_INVALID_ARG, "plan is null");
+  plan->ev_start = (cudaEvent_t)ev_start;
+  plan->ev_mid = (cudaEvent_t)ev_attn_done;
+  plan->ev_end = (cudaEvent_t)ev_end;
+  return HPC_OK;
+}
+
+hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
+                           const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                           const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                           hpc_tensor* lse, void* stream) {
+  return hpc_decode_attn_ex(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f,
+                            stream);
+}
+
+}  // extern "C"

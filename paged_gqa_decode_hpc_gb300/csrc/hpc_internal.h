@@ -1,0 +1,123 @@
+// Internal declarations of libhpc_decode.so (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "hpc_decode.h"
+
+namespace hpc {
+
+constexpr int kBlockTokens = 64;   // paged block = one tile of 64 tokens
+constexpr int kHeadDim = 128;
+constexpr int kGroup = 8;          // query heads per KV head
+constexpr int32_t kPlanMagic = 0x48504344;
+
+// Plan buffer words (device). Offsets of the variable arrays depend on the
+// plan's capacity, not on the step, so a device-built plan can be refilled
+// without moving anything:
+//   [0..7]            header (see hpc_decode_plan_export)
+//   part_seg_off      cap_parts + 1
+//   seq_seg_off       cap_seqs + 1
+//   cu_tiles          cap_seqs + 1   (device planner scratch; not exported)
+//   segs              4 * cap_segs
+enum HeaderWord { kMagic = 0, kKind, kNumSeqs, kNumParts, kNumTiles, kNumSegs, kNumSms,
+                  kSplits, kHeaderWords };
+
+struct PlanLayout {
+  int32_t cap_seqs = 0, cap_parts = 0, cap_segs = 0;
+  __host__ __device__ int64_t part_off() const { return kHeaderWords; }
+  __host__ __device__ int64_t seq_off() const { return part_off() + cap_parts + 1; }
+  __host__ __device__ int64_t cu_off() const { return seq_off() + cap_seqs + 1; }
+  __host__ __device__ int64_t seg_off() const { return (cu_off() + cap_seqs + 1 + 3) & ~int64_t(3); }  // 16-B aligned
+  __host__ __device__ int64_t words() const { return seg_off() + 4LL * cap_segs; }
+};
+
+}  // namespace hpc
+
+struct hpc_plan_s {
+  int32_t kind = HPC_PLAN_DYNAMIC;
+  int32_t device = 0;
+  hpc::PlanLayout layout;
+  int32_t num_sms = 0;        // CTAs the plan was sized for (dynamic grid)
+  int32_t max_seqs = 0;
+  // Host-side knowledge of the current step (always known: the caller passes
+  // num_seqs; the part/segment counts are known for host-built plans).
+  int32_t num_seqs = 0;
+  int32_t host_num_parts = -1;   // -1: only the device knows (device planner)
+  int32_t host_num_segs = -1;
+  int32_t static_kv_heads = 0;   // static plans: grid.y
+  int32_t* d_words = nullptr;    // plan buffer
+  int32_t* h_pinned = nullptr;   // staging for hpc_decode_plan_update
+  cudaEvent_t copy_done = nullptr;  // last upload from h_pinned
+  int32_t* d_err = nullptr;      // device error word
+  float* d_ws = nullptr;         // partial workspace: o [cap_segs][H_q][128], m, l
+  int64_t ws_heads = 0;          // H_q the workspace was sized for
+  cudaEvent_t ev_start = nullptr, ev_mid = nullptr, ev_end = nullptr;  // optional timing
+};
+
+namespace hpc {
+
+// Kernel parameter block of the attention kernel (passed by value).
+struct AttnParams {
+  const __nv_bfloat16* q;
+  int64_t q_sb, q_sh;           // strides (elements) of q over b, head
+  __nv_bfloat16* out;
+  int64_t o_sb, o_sh;
+  float* lse;                   // may be null
+  int64_t l_sb, l_sh;
+  const int32_t* block_table;
+  int64_t bt_sb;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* plan;          // plan buffer words
+  int32_t seq_off, seg_off, part_off, cu_off;  // word offsets in the plan buffer
+  int32_t num_seqs, num_q_heads, num_kv_heads, num_blocks;
+  int32_t static_mode;          // 1: blockIdx.x = segment, blockIdx.y = kv head
+  int32_t kv_swap;              // tensor map dims are (d, head, slot, block)
+  float score_scale_log2;       // softmax_scale * log2(e) (* k_scale for FP8)
+  float v_scale;                // FP8 V scale (1 for BF16)
+  float* ws_o;                  // [cap_segs][H_q][128]
+  float* ws_m;                  // [cap_segs][H_q]  (log2 domain)
+  float* ws_l;                  // [cap_segs][H_q]
+  int32_t* err;
+  unsigned long long timeout_ns;
+};
+
+struct MergeParams {
+  __nv_bfloat16* out;
+  int64_t o_sb, o_sh;
+  float* lse;
+  int64_t l_sb, l_sh;
+  const int32_t* plan;
+  int32_t seq_off, seg_off;
+  int32_t num_seqs, num_q_heads;
+  const float* ws_o;
+  const float* ws_m;
+  const float* ws_l;
+};
+
+// Host planners (plan_host.cu). Fill `words` (canonical layout sized by the
+// returned length) or report an error message.
+hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                             int32_t* words, const PlanLayout& L, std::string* err);
+hpc_status plan_static_host(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                            int32_t num_kv_heads, int32_t num_splits,
+                            int32_t** words_out, PlanLayout* L_out, std::string* err);
+int64_t dynamic_max_segs(int32_t num_seqs, int32_t num_parts);
+
+// Launchers (kernels .cu files).
+cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                               int32_t* words, const PlanLayout& L, int32_t* err,
+                               cudaStream_t stream);
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                             bool fp8, int grid_x, int grid_y, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_t stream);
+
+void set_error(const std::string& msg);
+
+}  // namespace hpc
