@@ -146,6 +146,38 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Bounded wait until the producer has issued unit `unit` into its slot. A
+// slot's successive rounds are consumed by different warps, so a warp may ask
+// for round r while the slot's barrier has completed only round r-2; the
+// mbarrier parity cannot tell those apart. Once the slot's issued word equals
+// the unit, rounds < r have completed and round r+1 cannot start before this
+// warp releases the slot, so the parity wait that follows is exact.
+__device__ __forceinline__ bool wait_issued(uint32_t word, uint32_t unit, volatile int* abort_flag,
+                                            int32_t* err, unsigned long long limit_ns) {
+  if (ld_acquire_shared(word) == unit) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_shared(word) == unit) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        atomicOr(err, HPC_DEVCHK_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait on an mbarrier phase. Returns false when the CTA is aborting
 // or the time limit passed (then the abort flag and the error bit are set).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -179,7 +211,8 @@ struct KernelCfg {
   static constexpr int kThreads = (NC + 1) * 32;
   static constexpr int kBarOff = STAGES * Geom<FP8>::kStageBytes;
   static constexpr int kAbortOff = kBarOff + 2 * STAGES * 8;
-  static constexpr int kCombOff = kAbortOff + 16;
+  static constexpr int kIssuedOff = kAbortOff + 16;  // u32 per slot: last unit issued
+  static constexpr int kCombOff = kIssuedOff + ((4 * STAGES + 15) / 16) * 16;
   static constexpr int kSmemBytes =
       1024 /* alignment slack */ + kCombOff + (COMBINE ? NC * 32 * kCombineFloats * 4 : 0);
 };
@@ -430,6 +463,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   const uint32_t bar_full = smem_base + Cfg::kBarOff;
   const uint32_t bar_empty = bar_full + STAGES * 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kAbortOff);
+  const uint32_t issued_word = smem_base + Cfg::kIssuedOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -456,6 +490,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       mbar_init(bar_empty + 8 * s, 1);
     }
     *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s)
+      reinterpret_cast<volatile uint32_t*>(smem + Cfg::kIssuedOff)[s] = 0xFFFFFFFFu;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -510,6 +546,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                 tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
                 tma_load_4d(dv + 8192, &tmv, fb, 64, c1, c2, bk, policy);
               }
+              st_release_shared(issued_word + 4 * slot, g);
               issued = g + 1;
             }
           }
@@ -556,8 +593,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           const uint32_t gu = gbase + (uint32_t)(i * hpass + hl);
           const uint32_t slot = gu % STAGES;
           if (dead) continue;
-          const bool ok = wait_phase(bar_full + 8 * slot, (gu / STAGES) & 1u, abort_flag, p.err,
-                                     p.timeout_ns);
+          const bool ok =
+              wait_issued(issued_word + 4 * slot, gu, abort_flag, p.err, p.timeout_ns) &&
+              wait_phase(bar_full + 8 * slot, (gu / STAGES) & 1u, abort_flag, p.err,
+                         p.timeout_ns);
           if (!__all_sync(0xffffffffu, ok)) {  // warp-uniform decision
             dead = true;
             continue;
