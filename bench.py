@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--scale-lengths", type=float, default=1.0,
+                    help="scale every KV length of the config (smaller profiling cases)")
     return ap.parse_args()
 
 
@@ -189,6 +191,17 @@ def max_over_ranks(ws, value):
     return float(t.item())
 
 
+def load_workload(args):
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+    if args.scale_lengths == 1.0:
+        return W.make_workload(args.config)
+    cfg = W.CONFIG_BY_NAME[args.config]
+    import torch
+    lens = W.draw_lengths(cfg, torch.Generator().manual_seed(cfg.seed))
+    lens = [max(1, int(round(L * args.scale_lengths))) for L in lens]
+    return W.make_workload(cfg, lengths=lens)
+
+
 # ------------------------------------------------------------ CPU oracle leg
 def oracle_sample(w, budget_s=4.0):
     """A bounded sample of the workload for the oracle: whole sequences, taken
@@ -243,7 +256,7 @@ def run_reference(args, ws, rank):
         return
     import oracle
     from paged_gqa_decode_hpc_gb300 import workloads as W
-    w = W.make_workload(args.config)
+    w = load_workload(args)
     budget = max(0.5, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
     sample, seqs = oracle_sample(w, budget_s=budget)
     time_oracle(sample, args.warmup)
@@ -284,7 +297,7 @@ def run_hpc(args, ws, rank, local):
         raise SystemExit("bench.py needs a CUDA GPU (the product path has no CPU fallback)")
     hpc.load_library()
     dev = torch.device("cuda", local)
-    w = W.make_workload(args.config)
+    w = load_workload(args)
     B, hq, hkv = w.num_seqs, w.num_q_heads, w.num_kv_heads
     fp8 = w.kv_dtype == "fp8_e4m3"
     q, kc, vc = w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev)
@@ -359,7 +372,9 @@ def run_hpc(args, ws, rank, local):
         "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V, shuffled block table; the pages' shapes)",
         "config": {
-            "workload": WORKLOAD_TEXT[args.config], "num_seqs": B,
+            "workload": WORKLOAD_TEXT[args.config] + (
+                f" (lengths scaled x{args.scale_lengths})" if args.scale_lengths != 1.0 else ""),
+            "num_seqs": B,
             "kv_tokens": int(w.seq_lens.sum()), "num_sms": num_sms,
             "algorithmic_bytes_per_step": nbytes,
             "l2": ("flushed between steps (write of 2x L2)" if flush is not None
