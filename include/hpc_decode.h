@@ -245,6 +245,40 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
 hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, void* ev_attn_done,
                                              void* ev_end);
 
+/*
+ * hpc_decode_attn_noalloc -- one decode step (device planner, attention,
+ * merge) that allocates no memory at all. The pages have no counterpart of
+ * this call; it exists for callers that cannot call cudaMalloc/cudaFree:
+ * code running inside an engine's enqueue step or a plugin whose contract
+ * forbids allocation there, and code whose device memory is all owned by a
+ * caching allocator, where a direct cudaMalloc/cudaFree would synchronise the
+ * device or fail under memory pressure.
+ *
+ * Its work list, partial results and error word live in one file-scope
+ * device array of about 13.9 MB that every GPU loading this library holds
+ * until the process exits. Limits (HPC_ERR_INVALID_ARG beyond them, with a
+ * message): num_seqs <= HPC_NOALLOC_MAX_SEQS, CTAs <= HPC_NOALLOC_MAX_CTAS,
+ * num_q_heads <= HPC_NOALLOC_MAX_Q_HEADS.
+ *
+ *   q, k_cache, v_cache, block_table, seq_lens, out, lse: as hpc_decode_attn
+ *               (seq_lens on the device; the plan is built from them here)
+ *   num_sms     CTAs of the persistent grid; <= 0 uses the device's SM count
+ *   device_error  device int32 receiving HPC_DEVCHK_* bits by atomic OR (the
+ *               caller zeroes it), or NULL to discard them
+ * The first call on each device looks up the array's device address for that
+ * device (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture. Every call uses the same array and it keeps the
+ * last call's contents, so calls whose work overlaps on the GPU (other
+ * streams, other threads) race with each other: order them on one stream.
+ */
+#define HPC_NOALLOC_MAX_SEQS 256
+#define HPC_NOALLOC_MAX_CTAS 160
+#define HPC_NOALLOC_MAX_Q_HEADS 64
+hpc_status hpc_decode_attn_noalloc(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                   const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                   const hpc_tensor* seq_lens, int32_t num_sms, hpc_tensor* out,
+                                   hpc_tensor* lse, int32_t* device_error, void* stream);
+
 /* hpc_device_sm_count -- streaming multiprocessors of the current device. */
 hpc_status hpc_device_sm_count(int32_t* num_sms);
 

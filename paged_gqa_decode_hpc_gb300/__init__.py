@@ -24,7 +24,7 @@ __all__ = [
     "hpc_decode_plan_device", "hpc_decode_plan_update", "hpc_decode_plan_export",
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
-    "hpc_decode_plan_set_timing_events",
+    "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
 ]
@@ -98,6 +98,7 @@ def load_library():
             "hpc_decode_attn_ex": [T, T, T, T, T, P, T, T, ctypes.c_float, P],
             "hpc_device_sm_count": [pi32],
             "hpc_decode_plan_set_timing_events": [P, P, P, P],
+            "hpc_decode_attn_noalloc": [T, T, T, T, T, i32, T, T, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -311,3 +312,27 @@ def hpc_decode_attn(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, out,
                                 ctypes.c_float(-1.0 if softmax_scale is None else softmax_scale),
                                 _stream_ptr(stream))
     _check(st)
+
+
+def hpc_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, out, lse=None,
+                            num_sms: int = 0, device_error=None, stream=None,
+                            k_scale: float = 1.0, v_scale: float = 1.0):
+    """One decode step (planner, attention, merge) that allocates nothing.
+
+    For callers that may not call cudaMalloc/cudaFree at this point -- an
+    engine's enqueue step or a plugin whose contract forbids allocation, or
+    code whose device memory is all owned by a caching allocator. The step's
+    scratch is a fixed device array inside the library (limits:
+    HPC_NOALLOC_MAX_SEQS sequences, HPC_NOALLOC_MAX_CTAS CTAs,
+    HPC_NOALLOC_MAX_Q_HEADS query heads). Calls that overlap on the GPU race
+    on that array; keep them on one stream. `device_error`: optional int32
+    CUDA tensor of one element receiving device-check bits (zero it first).
+    """
+    lib = load_library()
+    tq, tk, tv = make_tensor(q), make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
+    tb, ts, to = make_tensor(block_table), make_tensor(seq_lens), make_tensor(out)
+    tl = make_tensor(lse)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    err = ctypes.c_void_p(device_error.data_ptr()) if device_error is not None else None
+    _check(lib.hpc_decode_attn_noalloc(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), int(num_sms),
+                                       ref(to), ref(tl), err, _stream_ptr(stream)))
