@@ -1,4 +1,4 @@
-// Split-KV paged GQA decode attention for sm_103a, and the log-sum-exp merge.
+// Split-KV paged GQA decode attention for sm_103a (the merge pass is in merge_kernel.cu).
 //
 // The method ("vLLM x HPC-Ops", section "Attention Backend: Dynamic
 // Load-Balanced Scheduling"): a persistent grid whose CTAs each walk a list
@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 
 #include "hpc_internal.h"
+#include "ptx.cuh"
 
 namespace hpc {
 
@@ -467,6 +468,26 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Prologue that needs nothing from the preceding kernel: it overlaps that
+  // kernel's tail when launched with programmatic stream serialization.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s)
+      reinterpret_cast<volatile uint32_t*>(smem + Cfg::kIssuedOff)[s] = 0xFFFFFFFFu;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == NC && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+  }
+  griddep_wait();  // the plan (and inputs) of the preceding kernels are visible
+  griddep_launch_dependents();
+
   int seg_begin, seg_end, h_begin, h_count;
   if (p.static_mode) {
     seg_begin = blockIdx.x;
@@ -483,18 +504,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   const int hpass = h_count < NC ? h_count : NC;  // kv heads processed together
   const int npass = h_count / hpass;
   const int wph = NC / hpass;                     // consumer warps per kv head
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
-    }
-    *abort_flag = 0;
-    for (int s = 0; s < STAGES; ++s)
-      reinterpret_cast<volatile uint32_t*>(smem + Cfg::kIssuedOff)[s] = 0xFFFFFFFFu;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
   __syncthreads();
 
   if (warp == NC) {
@@ -676,67 +685,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   (void)c;
 }
 
-// ------------------------------------------------------------------ merge
-constexpr int kMergeThreads = 256;  // 8 query heads x 32 lanes x 4 dims
-
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p) {
-  const int b = blockIdx.x, hk = blockIdx.y;
-  const int s0 = p.plan[p.seq_off + b], s1 = p.plan[p.seq_off + b + 1];
-  const int ns = s1 - s0;
-  if (ns == 1) return;  // written by the attention kernel
-  const int j = hk * kGroup + (threadIdx.x >> 5);
-  const int d0 = (threadIdx.x & 31) * 4;
-  __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh + d0;
-  float* lse = p.lse ? p.lse + (int64_t)b * p.l_sb + (int64_t)j * p.l_sh : nullptr;
-  float M = -INFINITY;
-  for (int s = s0; s < s1; ++s) M = fmaxf(M, p.ws_m[(int64_t)s * p.num_q_heads + j]);
-  if (ns == 0 || M == -INFINITY) {
-    // empty sequence: out = 0, lse = -inf
-    *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
-    if (lse && (threadIdx.x & 31) == 0) *lse = -INFINITY;
-    return;
-  }
-  float l = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  constexpr int U = 8;
-  int s = s0;
-  for (; s + U <= s1; s += U) {
-    float mm[U], ll[U];
-    float4 oo[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t r = (int64_t)(s + u) * p.num_q_heads + j;
-      mm[u] = p.ws_m[r];
-      ll[u] = p.ws_l[r];
-      oo[u] = *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + d0);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float w = ex2(mm[u] - M);
-      l += ll[u] * w;
-      a0 += oo[u].x * w;
-      a1 += oo[u].y * w;
-      a2 += oo[u].z * w;
-      a3 += oo[u].w * w;
-    }
-  }
-  for (; s < s1; ++s) {
-    const int64_t r = (int64_t)s * p.num_q_heads + j;
-    const float w = ex2(p.ws_m[r] - M);
-    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + d0);
-    l += p.ws_l[r] * w;
-    a0 += v.x * w;
-    a1 += v.y * w;
-    a2 += v.z * w;
-    a3 += v.w * w;
-  }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(a0 * inv, a1 * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(a2 * inv, a3 * inv);
-  *reinterpret_cast<uint2*>(o) =
-      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-  if (lse && (threadIdx.x & 31) == 0) *lse = l > 0.f ? (M + __log2f(l)) * kLn2 : -INFINITY;
-}
-
 template <bool FP8, int STAGES, int NC, bool COMBINE>
 cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int gx,
                        int gy, cudaStream_t stream) {
@@ -749,8 +697,17 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtenso
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<dim3(gx, gy), Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, tk, tv);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(gx, gy);
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, tk, tv);
 }
 
 }  // namespace
@@ -765,12 +722,6 @@ cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const C
   }
   return combine ? launch_cfg<false, 5, 8, true>(p, tk, tv, gx, gy, stream)
                  : launch_cfg<false, 6, 8, false>(p, tk, tv, gx, gy, stream);
-}
-
-cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_t stream) {
-  if (p.num_seqs == 0) return cudaSuccess;
-  merge_kernel<<<dim3(p.num_seqs, num_kv_heads), kMergeThreads, 0, stream>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace hpc
