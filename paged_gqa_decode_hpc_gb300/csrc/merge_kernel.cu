@@ -9,11 +9,13 @@
 // "Attention Backend: Dynamic Load-Balanced Scheduling") but print no merge;
 // this is the standard identity that makes the split softmax exact.
 //
-// One CTA per (sequence, query head): 8 warps take the sequence's partials
-// round-robin, each lane owns 4 of the 128 output columns; every warp keeps a
-// running (M, l, o) and prefetches its next partials, and the warps' states
-// are combined in shared memory. A sequence with no tiles gets out = 0 and
-// lse = -inf here; a sequence finished inside one CTA is skipped.
+// One CTA of 4 warps per (sequence, query head). A warp takes every 4th
+// partial; per round of up to 32 partials each lane loads one partial's
+// (m, l) while the o rows are fetched in batches of 8 (each lane owns 4 of the
+// 128 columns), so a round costs about two memory round trips. The warps'
+// running (M, l, o) states are combined in shared memory. A sequence with no
+// tiles gets out = 0 and lse = -inf here; a sequence finished inside one CTA
+// is skipped.
 #include <cuda_bf16.h>
 
 #include "hpc_internal.h"
@@ -23,25 +25,18 @@ namespace hpc {
 
 namespace {
 
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 4;
 constexpr float kLn2f = 0.6931471805599453f;
 
-struct State {
-  float m, l;
-  float4 o;
-};
-
-__device__ __forceinline__ void absorb(State& st, float mi, float li, const float4& oi) {
-  if (mi == -INFINITY) return;  // empty partial
-  const float mn = fmaxf(st.m, mi);
-  const float a = st.m == -INFINITY ? 0.f : ptx_ex2(st.m - mn);
-  const float b = ptx_ex2(mi - mn);
-  st.m = mn;
-  st.l = st.l * a + li * b;
-  st.o.x = st.o.x * a + oi.x * b;
-  st.o.y = st.o.y * a + oi.y * b;
-  st.o.z = st.o.z * a + oi.z * b;
-  st.o.w = st.o.w * a + oi.w * b;
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
@@ -62,42 +57,69 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     }
     return;
   }
-  State st{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
-  constexpr int U = 4;
-  int s = s0 + warp;
-  for (; s + (U - 1) * kMergeWarps < s1; s += U * kMergeWarps) {
-    float mm[U], ll[U];
-    float4 oo[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t r = (int64_t)(s + u * kMergeWarps) * p.num_q_heads + j;
-      mm[u] = p.ws_m[r];
-      ll[u] = p.ws_l[r];
-      oo[u] = *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + 4 * lane);
+  const int64_t hq = p.num_q_heads;
+  const float* obase = p.ws_o + (int64_t)j * kHeadDim + 4 * lane;
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // this warp's partials: s0 + warp + kMergeWarps * t, t = 0, 1, ...
+  const int mine = (ns - warp + kMergeWarps - 1) / kMergeWarps;
+  for (int r0 = 0; r0 < mine; r0 += 32) {
+    const int cnt = mine - r0 < 32 ? mine - r0 : 32;
+    const int64_t my_s = s0 + warp + (int64_t)kMergeWarps * (r0 + lane);
+    float mk = -INFINITY, lk = 0.f;
+    if (lane < cnt) {
+      mk = p.ws_m[my_s * hq + j];
+      lk = p.ws_l[my_s * hq + j];
     }
+    const float Mn = fmaxf(M, warp_max(mk));
+    if (Mn == -INFINITY) continue;  // only empty partials so far
+    const float scale = M == -INFINITY ? 0.f : ptx_ex2(M - Mn);
+    const float wk = mk == -INFINITY ? 0.f : ptx_ex2(mk - Mn);
+    L = L * scale + warp_sum(lk * wk);
+    acc.x *= scale; acc.y *= scale; acc.z *= scale; acc.w *= scale;
+    M = Mn;
+    for (int k0 = 0; k0 < cnt; k0 += 8) {
+      float4 v[8];
 #pragma unroll
-    for (int u = 0; u < U; ++u) absorb(st, mm[u], ll[u], oo[u]);
+      for (int u = 0; u < 8; ++u) {
+        const int64_t s = s0 + warp + (int64_t)kMergeWarps * (r0 + k0 + u);
+        v[u] = k0 + u < cnt ? *reinterpret_cast<const float4*>(obase + s * hq * kHeadDim)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wk, (k0 + u) & 31);
+        acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+      }
+    }
   }
-  for (; s < s1; s += kMergeWarps) {
-    const int64_t r = (int64_t)s * p.num_q_heads + j;
-    absorb(st, p.ws_m[r], p.ws_l[r], *reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim + 4 * lane));
-  }
-  s_o[warp][lane] = st.o;
+  s_o[warp][lane] = acc;
   if (lane == 0) {
-    s_m[warp] = st.m;
-    s_l[warp] = st.l;
+    s_m[warp] = M;
+    s_l[warp] = L;
   }
   __syncthreads();
   if (warp != 0) return;
-  State t{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  float Mt = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) absorb(t, s_m[w], s_l[w], s_o[w][lane]);
-  const float inv = t.l > 0.f ? 1.f / t.l : 0.f;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(t.o.x * inv, t.o.y * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(t.o.z * inv, t.o.w * inv);
+  for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
+  float Lt = 0.f;
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (Mt != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      const float f = s_m[w] == -INFINITY ? 0.f : ptx_ex2(s_m[w] - Mt);
+      Lt += s_l[w] * f;
+      t.x += s_o[w][lane].x * f; t.y += s_o[w][lane].y * f;
+      t.z += s_o[w][lane].z * f; t.w += s_o[w][lane].w * f;
+    }
+  }
+  const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(t.z * inv, t.w * inv);
   *reinterpret_cast<uint2*>(o) =
       make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-  if (lse && lane == 0) *lse = t.l > 0.f ? (t.m + __log2f(t.l)) * kLn2f : -INFINITY;
+  if (lse && lane == 0) *lse = Lt > 0.f ? (Mt + __log2f(Lt)) * kLn2f : -INFINITY;
 }
 
 }  // namespace

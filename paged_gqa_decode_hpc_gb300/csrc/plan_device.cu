@@ -6,10 +6,10 @@
 //   part start  s_p = floor(p*T/P),   part of tile x = floor(((x+1)*P - 1)/T),
 // so the results agree bit for bit.
 //
-// One CTA of 1024 threads walks the sequences in chunks of 1024 with two
-// block-wide scans (tile counts, then segments per sequence). The prefix
-// arrays are kept in shared memory when they fit, so the per-part searches
-// never wait on global memory.
+// One CTA of 1024 threads: two block-wide scans (tile counts, then segments
+// per sequence), then one thread per segment and one per part, each locating
+// its sequence by binary search. The prefix arrays are kept in shared memory
+// when they fit, so the searches never wait on global memory.
 #include "hpc_internal.h"
 #include "ptx.cuh"
 
@@ -20,12 +20,17 @@ namespace {
 constexpr int kPlanThreads = 1024;
 constexpr int kSmemSeqs = 6000;  // 2 * (6000 + 1) int32 fit the default 48 KB
 
-__device__ __forceinline__ int64_t dpart_start(int64_t p, int64_t T, int64_t P) {
-  return (p * T) / P;
-}
-__device__ __forceinline__ int64_t dpart_of(int64_t x, int64_t T, int64_t P) {
-  return ((x + 1) * P - 1) / T;
-}
+// floor(p*T/P) and the part owning tile x; 32-bit division when products fit.
+struct PartMath {
+  int64_t T, P;
+  bool small;
+  __device__ __forceinline__ int64_t start(int64_t p) const {
+    return small ? (int64_t)((uint32_t)(p * T) / (uint32_t)P) : (p * T) / P;
+  }
+  __device__ __forceinline__ int64_t of(int64_t x) const {
+    return small ? (int64_t)((uint32_t)((x + 1) * P - 1) / (uint32_t)T) : ((x + 1) * P - 1) / T;
+  }
+};
 
 // Inclusive block scan of one int per thread; returns the block total too.
 __device__ __forceinline__ int32_t block_inclusive_scan(int32_t v, int32_t* warp_tot,
@@ -111,8 +116,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
   }
   const int64_t T = carry;
   const int64_t P = T < num_sms ? T : num_sms;
+  PartMath pm{T, P, (T + 1) * (P + 1) < (int64_t)UINT32_MAX};
 
-  // 2. segments per sequence -> seq_seg_off, and 3. the segments themselves
+  // 2. segments per sequence -> seq_seg_off
   if (tid == 0) {
     so[0] = 0;
     so_g[0] = 0;
@@ -121,45 +127,50 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
   for (int32_t base = 0; base < B; base += kPlanThreads) {
     const int32_t b = base + tid;
     int32_t cnt = 0;
-    int64_t pf = 0, lo_b = 0, hi_b = 0;
     if (b < B) {
-      lo_b = cu[b];
-      hi_b = cu[b + 1];
-      if (hi_b > lo_b) {
-        pf = dpart_of(lo_b, T, P);
-        cnt = (int32_t)(dpart_of(hi_b - 1, T, P) - pf + 1);
-      }
+      const int64_t lo_b = cu[b], hi_b = cu[b + 1];
+      if (hi_b > lo_b) cnt = (int32_t)(pm.of(hi_b - 1) - pm.of(lo_b) + 1);
     }
     int32_t chunk_total;
     const int32_t incl = block_inclusive_scan(cnt, warp_tot, &chunk_total);
     if (b < B) {
-      const int64_t first = gcarry + incl - cnt;
-      so[b + 1] = (int32_t)(first + cnt);
-      if (staged) so_g[b + 1] = (int32_t)(first + cnt);
-      for (int32_t j = 0; j < cnt; ++j) {
-        const int64_t p = pf + j;
-        const int64_t s0 = dpart_start(p, T, P), s1 = dpart_start(p + 1, T, P);
-        int4 rec;
-        rec.x = b;
-        rec.y = (int32_t)((lo_b > s0 ? lo_b : s0) - lo_b);
-        rec.z = (int32_t)((hi_b < s1 ? hi_b : s1) - lo_b);
-        rec.w = cnt == 1 ? HPC_SEG_WHOLE : 0;
-        *reinterpret_cast<int4*>(segs + 4 * (first + j)) = rec;
-      }
+      so[b + 1] = (int32_t)(gcarry + incl);
+      if (staged) so_g[b + 1] = (int32_t)(gcarry + incl);
     }
     gcarry += chunk_total;
   }
   __syncthreads();
+  const int32_t S = (int32_t)gcarry;
+
+  // 3. the segments, one thread each: sequence = last b with so[b] <= g
+  for (int32_t g = tid; g < S; g += kPlanThreads) {
+    int32_t lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int32_t mid = (lo + hi) >> 1;
+      if (so[mid] <= g) lo = mid; else hi = mid;
+    }
+    const int32_t b = lo, j = g - so[b];
+    const int64_t lo_b = cu[b], hi_b = cu[b + 1];
+    const int32_t cnt = so[b + 1] - so[b];
+    const int64_t p = pm.of(lo_b) + j;
+    const int64_t s0 = pm.start(p), s1 = pm.start(p + 1);
+    int4 rec;
+    rec.x = b;
+    rec.y = (int32_t)((lo_b > s0 ? lo_b : s0) - lo_b);
+    rec.z = (int32_t)((hi_b < s1 ? hi_b : s1) - lo_b);
+    rec.w = cnt == 1 ? HPC_SEG_WHOLE : 0;
+    *reinterpret_cast<int4*>(segs + 4 * (int64_t)g) = rec;
+  }
 
   // 4. first segment of each part
   for (int64_t p = tid; p < P; p += kPlanThreads) {
-    const int32_t s = (int32_t)dpart_start(p, T, P);
+    const int32_t s = (int32_t)pm.start(p);
     int32_t lo = 0, hi = B;  // the last b with cu[b] <= s (a non-empty sequence)
     while (hi - lo > 1) {
       const int32_t mid = (lo + hi) >> 1;
       if (cu[mid] <= s) lo = mid; else hi = mid;
     }
-    part_off[p] = so[lo] + (int32_t)(p - dpart_of(cu[lo], T, P));
+    part_off[p] = so[lo] + (int32_t)(p - pm.of(cu[lo]));
   }
   if (tid == 0) {
     part_off[P] = (int32_t)gcarry;
