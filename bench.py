@@ -311,10 +311,15 @@ def run_hpc(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     nbytes = w.algorithmic_bytes()
     flush = None if args.no_flush else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = None if args.no_flush else torch.ones(2 * L2_BYTES // 4, dtype=torch.int32,
+                                                     device=dev)
 
     def flush_l2():
+        # Write 2x L2, then read another 2x L2 so that L2 ends up holding clean
+        # lines: no write-back of the flush lands inside the next timed step.
         if flush is not None:
             flush.fill_(1)
+            flush_rd.sum()
 
     def mk():
         e = torch.cuda.Event(enable_timing=True)
@@ -391,7 +396,7 @@ def run_hpc(args, ws, rank, local):
             "num_seqs": B,
             "kv_tokens": int(w.seq_lens.sum()), "num_sms": num_sms,
             "algorithmic_bytes_per_step": nbytes,
-            "l2": ("flushed between steps (write of 2x L2)" if flush is not None
+            "l2": ("flushed between steps (write 2x L2, then read 2x L2)" if flush is not None
                    else "not flushed"),
             "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
         },
