@@ -28,8 +28,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <cstdlib>
-
 #include "hpc_internal.h"
 #include "ptx.cuh"
 
@@ -79,15 +77,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
       "l"(policy)
-      : "memory");
-}
-// L2 prefetch of one tensor-map box (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                int c3) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -520,9 +509,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   if (warp == NC) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = evict_first_policy();
-    // L2 lookahead: about 256 KB of K/V per CTA ahead of the ring's loads.
-    constexpr int kPrefetchUnits = (256 * 1024) / kStage;
-    const int pf_tiles = (kPrefetchUnits + hpass - 1) / hpass;
     uint32_t g = 0, issued = 0;
     bool stop = false;
     for (int seg = seg_begin; seg < seg_end; ++seg) {
@@ -543,28 +529,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
               atomicOr(p.err, HPC_DEVCHK_TABLE_TOO_SHORT);
             }
           }
-          // block of the tile `pf_tiles` ahead, prefetched into L2 (-1: none)
-          int blkp = -1;
-          if (i + pf_tiles < n && tb + i + pf_tiles < p.max_blocks) {
-            const int v = __ldg(btrow + tb + i + pf_tiles);
-            if (v >= 0 && v < p.num_blocks) blkp = v;
-          }
           const int cnt = n - i0 < 32 ? n - i0 : 32;
           for (int ii = 0; ii < cnt; ++ii) {
             const int bk = __shfl_sync(0xffffffffu, blk, ii);
-            const int bkp = __shfl_sync(0xffffffffu, blkp, ii);
             for (int hl = 0; hl < hpass; ++hl, ++g) {
               if (lane != 0 || stop) continue;
               const int h = h_begin + pass * hpass + hl;
-              if (bkp >= 0) {
-                const int q1 = p.kv_swap ? h : 0, q2 = p.kv_swap ? 0 : h;
-                tma_prefetch_4d(&tmk, 0, q1, q2, bkp);
-                tma_prefetch_4d(&tmv, 0, q1, q2, bkp);
-                if constexpr (!FP8) {
-                  tma_prefetch_4d(&tmk, 64, q1, q2, bkp);
-                  tma_prefetch_4d(&tmv, 64, q1, q2, bkp);
-                }
-              }
               const uint32_t slot = g % STAGES;
               const uint32_t par = ((g / STAGES) & 1u) ^ 1u;
               if (!wait_phase(bar_empty + 8 * slot, par, abort_flag, p.err, p.timeout_ns)) {
@@ -742,30 +712,16 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-namespace {
-// Ring depth without the combine scratch: the default fills shared memory;
-// HPC_DECODE_DEEP_RING=0 selects one stage less (kept for measurements).
-bool deep_ring() {
-  static const bool v = [] {
-    const char* e = std::getenv("HPC_DECODE_DEEP_RING");
-    return !(e && e[0] == '0');
-  }();
-  return v;
-}
-}  // namespace
-
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              bool fp8, int gx, int gy, cudaStream_t stream) {
   const int hc = p.static_mode ? 1 : p.num_kv_heads;
   const bool combine = hc < 8;
   if (fp8) {
-    if (combine) return launch_cfg<true, 10, 8, true>(p, tk, tv, gx, gy, stream);
-    return deep_ring() ? launch_cfg<true, 13, 8, false>(p, tk, tv, gx, gy, stream)
-                       : launch_cfg<true, 12, 8, false>(p, tk, tv, gx, gy, stream);
+    return combine ? launch_cfg<true, 10, 8, true>(p, tk, tv, gx, gy, stream)
+                   : launch_cfg<true, 12, 8, false>(p, tk, tv, gx, gy, stream);
   }
-  if (combine) return launch_cfg<false, 5, 8, true>(p, tk, tv, gx, gy, stream);
-  return deep_ring() ? launch_cfg<false, 7, 8, false>(p, tk, tv, gx, gy, stream)
-                     : launch_cfg<false, 6, 8, false>(p, tk, tv, gx, gy, stream);
+  return combine ? launch_cfg<false, 5, 8, true>(p, tk, tv, gx, gy, stream)
+                 : launch_cfg<false, 6, 8, false>(p, tk, tv, gx, gy, stream);
 }
 
 }  // namespace hpc
