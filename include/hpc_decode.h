@@ -228,6 +228,25 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
                            const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
                            hpc_tensor* lse, void* stream);
 
+/*
+ * hpc_decode_step -- one whole decode step on the device: the balanced plan
+ * of hpc_decode_plan_device, attention and merge, with the planning folded
+ * into the attention kernel's start (each CTA derives its own part from the
+ * device lengths), so a step is two kernel launches. Afterwards `plan` holds
+ * this step's work list, word for word the one hpc_decode_plan_device would
+ * write (hpc_decode_plan_export). Batches above 3072 sequences run the
+ * separate planner kernel first. Allocates nothing; may be captured in a
+ * CUDA graph after a first call outside the capture.
+ *   q, k_cache, v_cache, block_table, out, lse: as hpc_decode_attn
+ *   seq_lens  device int32 [B], contiguous
+ *   plan      from hpc_decode_plan_create with max_seqs >= B
+ *   num_sms   CTAs of the persistent grid, <= the plan's num_sms
+ */
+hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
+                           const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                           const hpc_tensor* seq_lens, hpc_plan_t plan, int32_t num_sms,
+                           hpc_tensor* out, hpc_tensor* lse, void* stream);
+
 /* hpc_decode_attn_ex -- hpc_decode_attn with an explicit softmax scale
  * (> 0; a value <= 0 selects 1/sqrt(head_dim)). */
 hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,

@@ -24,7 +24,7 @@ __all__ = [
     "hpc_decode_plan_device", "hpc_decode_plan_update", "hpc_decode_plan_export",
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
-    "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc",
+    "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc", "hpc_decode_step",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
 ]
@@ -99,6 +99,7 @@ def load_library():
             "hpc_device_sm_count": [pi32],
             "hpc_decode_plan_set_timing_events": [P, P, P, P],
             "hpc_decode_attn_noalloc": [T, T, T, T, T, i32, T, T, P, P],
+            "hpc_decode_step": [T, T, T, T, T, P, i32, T, T, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -291,6 +292,19 @@ def make_tensor(t, scale: float = 1.0) -> Optional[HpcTensor]:
         d.stride[i] = t.stride(i)
     d.scale = float(scale)
     return d
+
+
+def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int, out,
+                    lse=None, stream=None, k_scale: float = 1.0, v_scale: float = 1.0):
+    """One decode step (plan inside the attention kernel, attention, merge);
+    `plan` from hpc_decode_plan_create, `seq_lens` an int32 CUDA tensor."""
+    lib = load_library()
+    tq, tk, tv = make_tensor(q), make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
+    tb, ts, to = make_tensor(block_table), make_tensor(seq_lens), make_tensor(out)
+    tl = make_tensor(lse)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    _check(lib.hpc_decode_step(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), plan.handle,
+                               int(num_sms), ref(to), ref(tl), _stream_ptr(stream)))
 
 
 def hpc_decode_attn(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, out, lse=None,

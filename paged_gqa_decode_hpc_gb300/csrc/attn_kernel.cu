@@ -214,8 +214,92 @@ struct KernelCfg {
   static constexpr int kAbortOff = kBarOff + 2 * STAGES * 8;
   static constexpr int kIssuedOff = kAbortOff + 16;  // u32 per slot: last unit issued
   static constexpr int kCombOff = kIssuedOff + ((4 * STAGES + 15) / 16) * 16;
-  static constexpr int kSmemBytes =
-      1024 /* alignment slack */ + kCombOff + (COMBINE ? NC * 32 * kCombineFloats * 4 : 0);
+  static constexpr int kPlanOff = kCombOff + (COMBINE ? NC * 32 * kCombineFloats * 4 : 0);
+  static constexpr int kSmemBytes = 1024 /* alignment slack */ + kPlanOff;
+  // with a fused plan: + 2 * (B + 1) int32 prefix arrays
+  static constexpr int kSmemBytesFused = kSmemBytes + 8 * (kFusedPlanMaxSeqs + 1);
+};
+
+// Part arithmetic of the balanced plan: part start floor(p*T/P) and the part
+// owning tile x, floor(((x+1)*P - 1)/T); 32-bit division when products fit.
+struct PartMath {
+  int64_t T, P;
+  bool small;
+  __device__ __forceinline__ int64_t start(int64_t q) const {
+    return small ? (int64_t)((uint32_t)(q * T) / (uint32_t)P) : (q * T) / P;
+  }
+  __device__ __forceinline__ int64_t of(int64_t x) const {
+    return small ? (int64_t)((uint32_t)((x + 1) * P - 1) / (uint32_t)T) : ((x + 1) * P - 1) / T;
+  }
+};
+
+// Inclusive scan of one value per thread over the whole CTA (any size <= 1024).
+__device__ __forceinline__ int32_t cta_inclusive_scan(int32_t v, int32_t* warp_tot,
+                                                      int32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int32_t res = v + (warp > 0 ? warp_tot[warp - 1] : 0);
+  *total = warp_tot[nwarps - 1];
+  __syncthreads();
+  return res;
+}
+
+// The segments of one CTA, read from a plan in global memory or derived from
+// the prefix arrays (tiles cu[], segments so[]) of a plan built in the CTA.
+struct SegCursor {
+  bool fused;
+  // plan in global memory
+  const int32_t* recs;
+  int seg, seg_end;
+  // plan built in the CTA
+  const int32_t* cu;
+  const int32_t* so;
+  PartMath pm;
+  int part, cur, B;
+  int32_t s_lo, s_hi;
+
+  __device__ __forceinline__ bool next(int& b, int& tb, int& te, bool& whole, int& slot) {
+    if (!fused) {
+      if (seg >= seg_end) return false;
+      const int4 rec = *reinterpret_cast<const int4*>(recs + 4 * seg);
+      b = rec.x;
+      tb = rec.y;
+      te = rec.z;
+      whole = (rec.w & HPC_SEG_WHOLE) != 0;
+      slot = seg++;
+      return true;
+    }
+    while (cur < B) {
+      const int32_t lo_b = cu[cur], hi_b = cu[cur + 1];
+      if (lo_b >= s_hi) return false;
+      const int bb = cur++;
+      if (hi_b <= s_lo || hi_b == lo_b) continue;
+      b = bb;
+      tb = (lo_b > s_lo ? lo_b : s_lo) - lo_b;
+      te = (hi_b < s_hi ? hi_b : s_hi) - lo_b;
+      whole = so[bb + 1] - so[bb] == 1;
+      slot = so[bb] + (int)(part - pm.of(lo_b));
+      return true;
+    }
+    return false;
+  }
 };
 
 // Output coordinate of accumulator element (dm, r): BF16 rows are d = 16dm+g
@@ -488,16 +572,102 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   griddep_wait();  // the plan (and inputs) of the preceding kernels are visible
   griddep_launch_dependents();
 
-  int seg_begin, seg_end, h_begin, h_count;
+  SegCursor cur0;
+  cur0.fused = false;
+  cur0.recs = p.plan + p.seg_off;
+  int h_begin, h_count;
   if (p.static_mode) {
-    seg_begin = blockIdx.x;
-    seg_end = seg_begin + 1;
+    cur0.seg = blockIdx.x;
+    cur0.seg_end = cur0.seg + 1;
     h_begin = blockIdx.y;
     h_count = 1;
-  } else {
+  } else if (!p.fused_plan) {
     if ((int)blockIdx.x >= p.plan[kNumParts]) return;  // fewer parts than CTAs
-    seg_begin = p.plan[p.part_off + blockIdx.x];
-    seg_end = p.plan[p.part_off + blockIdx.x + 1];
+    cur0.seg = p.plan[p.part_off + blockIdx.x];
+    cur0.seg_end = p.plan[p.part_off + blockIdx.x + 1];
+    h_begin = 0;
+    h_count = p.num_kv_heads;
+  } else {
+    // ---- plan this step inside the CTA (same closed forms as the planners)
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t s_bad;
+    int32_t* cu = reinterpret_cast<int32_t*>(smem + Cfg::kPlanOff);
+    int32_t* so = cu + (p.num_seqs + 1);
+    const int B = p.num_seqs, nt = blockDim.x, tid = threadIdx.x;
+    if (tid == 0) {
+      s_bad = 0;
+      cu[0] = 0;
+      so[0] = 0;
+    }
+    __syncthreads();
+    int64_t carry = 0;
+    for (int base = 0; base < B; base += nt) {
+      const int b = base + tid;
+      int32_t n = 0;
+      if (b < B) {
+        const int32_t len = p.seq_lens[b];
+        if (len < 0) s_bad = 1;
+        n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) : 0;
+      }
+      int32_t tot;
+      const int32_t incl = cta_inclusive_scan(n, warp_tot, &tot);
+      if (b < B) cu[b + 1] = (int32_t)(carry + incl);
+      carry += tot;
+    }
+    __syncthreads();
+    const bool bad = s_bad || carry > INT32_MAX;
+    const int64_t T = bad ? 0 : carry;
+    const int64_t P = T < p.plan_num_sms ? T : p.plan_num_sms;
+    PartMath pm{T, P, (T + 1) * (P + 1) < (int64_t)UINT32_MAX};
+    int64_t gcarry = 0;
+    for (int base = 0; base < B; base += nt) {
+      const int b = base + tid;
+      int32_t cnt = 0;
+      if (b < B && !bad && cu[b + 1] > cu[b]) cnt = (int32_t)(pm.of(cu[b + 1] - 1) - pm.of(cu[b]) + 1);
+      int32_t tot;
+      const int32_t incl = cta_inclusive_scan(cnt, warp_tot, &tot);
+      if (b < B) so[b + 1] = (int32_t)(gcarry + incl);
+      gcarry += tot;
+    }
+    __syncthreads();
+    // this CTA's share of the plan words (read later by the merge and export)
+    int32_t* w = p.plan_out;
+    for (int b = blockIdx.x + gridDim.x * tid; b < B; b += gridDim.x * nt) {
+      w[p.cu_off + b + 1] = bad ? 0 : cu[b + 1];
+      w[p.seq_off + b + 1] = bad ? 0 : so[b + 1];
+    }
+    const int part = blockIdx.x;
+    if (!bad && part < P && tid == 0) {
+      const int32_t s0 = (int32_t)pm.start(part);
+      int lo = 0, hi = B;  // last b with cu[b] <= s0 (a non-empty sequence)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= s0) lo = mid; else hi = mid;
+      }
+      w[p.part_off + part] = so[lo] + (int32_t)(part - pm.of(cu[lo]));
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+      if (bad) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
+      w[kMagic] = kPlanMagic; w[kKind] = HPC_PLAN_DYNAMIC; w[kNumSeqs] = B;
+      w[kNumParts] = (int32_t)P; w[kNumTiles] = (int32_t)T; w[kNumSegs] = (int32_t)gcarry;
+      w[kNumSms] = p.plan_num_sms; w[kSplits] = 0;
+      w[p.cu_off] = 0; w[p.seq_off] = 0; w[p.part_off + P] = (int32_t)gcarry;
+    }
+    if (part >= P) return;  // uniform over the CTA
+    cur0.fused = true;
+    cur0.cu = cu;
+    cur0.so = so;
+    cur0.pm = pm;
+    cur0.part = part;
+    cur0.B = B;
+    cur0.s_lo = (int32_t)pm.start(part);
+    cur0.s_hi = (int32_t)pm.start(part + 1);
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= cur0.s_lo) lo = mid; else hi = mid;
+    }
+    cur0.cur = lo;
     h_begin = 0;
     h_count = p.num_kv_heads;
   }
@@ -511,9 +681,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     const uint64_t policy = evict_first_policy();
     uint32_t g = 0, issued = 0;
     bool stop = false;
-    for (int seg = seg_begin; seg < seg_end; ++seg) {
-      const int4 rec = *reinterpret_cast<const int4*>(p.plan + p.seg_off + 4 * seg);
-      const int b = rec.x, tb = rec.y, n = rec.z - rec.y;
+    SegCursor sc = cur0;
+    int b, tb, te, slot;
+    bool whole;
+    while (sc.next(b, tb, te, whole, slot)) {
+      const int n = te - tb;
+      if (sc.fused && lane == 0) {  // this part's segment records of the plan
+        int4 rec;
+        rec.x = b;
+        rec.y = tb;
+        rec.z = te;
+        rec.w = whole ? HPC_SEG_WHOLE : 0;
+        *reinterpret_cast<int4*>(p.plan_out + p.seg_off + 4 * (int64_t)slot) = rec;
+      }
       const int32_t* btrow = p.block_table + (int64_t)b * p.bt_sb;
       for (int pass = 0; pass < npass; ++pass) {
         for (int i0 = 0; i0 < n; i0 += 32) {
@@ -578,12 +758,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   const int c = lane & 3;
   uint32_t gbase = 0;
   bool dead = false;
-  for (int seg = seg_begin; seg < seg_end; ++seg) {
-    const int4 rec = *reinterpret_cast<const int4*>(p.plan + p.seg_off + 4 * seg);
-    const int b = rec.x, tb = rec.y, n = rec.z - rec.y;
-    const bool whole = (rec.w & HPC_SEG_WHOLE) != 0;
+  SegCursor sc = cur0;
+  int b, tb, te, seg;
+  bool whole;
+  while (sc.next(b, tb, te, whole, seg)) {
+    const int n = te - tb;
     const int len = p.seq_lens[b];
-    if (warp == 0 && lane == 0) {
+    if (!sc.fused && warp == 0 && lane == 0) {
       const int n_plan = p.plan[p.cu_off + b + 1] - p.plan[p.cu_off + b];
       const int n_dev = len > 0 ? (len + kBlockTokens - 1) / kBlockTokens : 0;
       if (n_plan != n_dev) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
@@ -692,15 +873,16 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtenso
   auto kern = attn_kernel<FP8, STAGES, NC, COMBINE>;
   static bool configured = false;  // per instantiation; attribute is per device function
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytesFused);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, gy);
   cfg.blockDim = dim3(Cfg::kThreads);
-  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.dynamicSmemBytes =
+      Cfg::kSmemBytes + (p.fused_plan ? 8 * ((size_t)p.num_seqs + 1) : 0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -404,10 +404,16 @@ void hpc_decode_plan_destroy(hpc_plan_t plan) {
   free_plan(plan);
 }
 
-hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
-                              const hpc_tensor* v_cache, const hpc_tensor* block_table,
-                              const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
-                              hpc_tensor* lse, float softmax_scale, void* stream) {
+}  // extern "C"
+
+namespace hpc {
+namespace {
+// Attention + merge. fused_num_sms > 0: the attention kernel plans the step
+// itself (P = min(fused_num_sms, T)) and writes the plan words into `plan`.
+hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_tensor* v_cache,
+                     const hpc_tensor* block_table, const hpc_tensor* seq_lens, hpc_plan_t plan,
+                     hpc_tensor* out, hpc_tensor* lse, float softmax_scale, void* stream,
+                     int32_t fused_num_sms) {
   hpc_status st;
   if ((st = check_tensor(q, "q", 3)) != HPC_OK) return st;
   if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
@@ -481,7 +487,9 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
 
   // grid
   int gx, gy = 1;
-  if (plan->kind == HPC_PLAN_STATIC) {
+  if (fused_num_sms > 0) {
+    gx = fused_num_sms;
+  } else if (plan->kind == HPC_PLAN_STATIC) {
     gx = plan->host_num_segs;
     gy = (int)Hkv;
   } else {
@@ -523,6 +531,9 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
     p.num_blocks = (int32_t)NB;
     p.static_mode = plan->kind == HPC_PLAN_STATIC;
     p.kv_swap = swap;
+    p.fused_plan = fused_num_sms > 0;
+    p.plan_num_sms = fused_num_sms;
+    p.plan_out = plan->d_words;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
     p.score_scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_cache->scale : 1.0f);
     p.v_scale = fp8 ? v_cache->scale : 1.0f;
@@ -560,6 +571,51 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
     return fail(HPC_ERR_CUDA, std::string("merge launch: ") + cudaGetErrorString(ce));
   if (plan->ev_end) HPC_CUDA_TRY(cudaEventRecord(plan->ev_end, s));
   return HPC_OK;
+}
+
+
+}  // namespace
+}  // namespace hpc
+
+extern "C" {
+
+hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
+                              const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                              const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                              hpc_tensor* lse, float softmax_scale, void* stream) {
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, softmax_scale,
+                   stream, 0);
+}
+
+hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
+                           const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                           const hpc_tensor* seq_lens, hpc_plan_t plan, int32_t num_sms,
+                           hpc_tensor* out, hpc_tensor* lse, void* stream) {
+  if (!plan || plan->kind != HPC_PLAN_DYNAMIC || !plan->h_pinned)
+    return fail(HPC_ERR_INVALID_ARG, "plan must come from hpc_decode_plan_create");
+  if (!q || !q->data || q->ndim != 3)
+    return fail(HPC_ERR_INVALID_ARG, "q must be a 3-D tensor [B][H_q][128]");
+  if (!seq_lens || !seq_lens->data || seq_lens->ndim != 1 || seq_lens->dtype != HPC_I32 ||
+      seq_lens->shape[0] != q->shape[0] || (q->shape[0] > 1 && seq_lens->stride[0] != 1))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous device int32 [B]");
+  const int64_t B = q->shape[0];
+  if (B > plan->layout.cap_seqs)
+    return fail(HPC_ERR_INVALID_ARG, "num_seqs exceeds the plan's max_seqs");
+  if (num_sms <= 0 || num_sms > plan->layout.cap_parts)
+    return fail(HPC_ERR_INVALID_ARG, "num_sms must be in [1, plan num_sms]");
+  if (B > kFusedPlanMaxSeqs || B == 0) {  // separate planner kernel
+    hpc_status st = hpc_decode_plan_device((const int32_t*)seq_lens->data, (int32_t)B, num_sms,
+                                           plan, stream);
+    if (st != HPC_OK) return st;
+    return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
+                     0);
+  }
+  plan->num_seqs = (int32_t)B;
+  plan->num_sms = num_sms;
+  plan->host_num_parts = -1;
+  plan->host_num_segs = -1;
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
+                   num_sms);
 }
 
 hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, void* ev_attn_done,

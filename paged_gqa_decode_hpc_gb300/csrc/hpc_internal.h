@@ -78,6 +78,10 @@ struct AttnParams {
   int32_t seq_off, seg_off, part_off, cu_off;  // word offsets in the plan buffer
   int32_t num_seqs, num_q_heads, num_kv_heads, num_blocks;
   int32_t static_mode;          // 1: blockIdx.x = segment, blockIdx.y = kv head
+  int32_t fused_plan;           // 1: each CTA plans its own part from seq_lens and
+                                //    the CTAs write the plan words (plan_out)
+  int32_t plan_num_sms;         // fused: parts cap (P = min(plan_num_sms, T))
+  int32_t* plan_out;            // fused: plan buffer written by the kernel
   int32_t kv_swap;              // tensor map dims are (d, head, slot, block)
   float score_scale_log2;       // softmax_scale * log2(e) (* k_scale for FP8)
   float v_scale;                // FP8 V scale (1 for BF16)
@@ -116,6 +120,9 @@ cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_
                                cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              bool fp8, int grid_x, int grid_y, cudaStream_t stream);
+// Largest batch the attention kernel can plan by itself (prefix arrays in
+// shared memory next to the K/V ring).
+constexpr int32_t kFusedPlanMaxSeqs = 3072;
 cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_t stream);
 
 void set_error(const std::string& msg);

@@ -1,0 +1,123 @@
+"""hpc_decode_step: the attention kernel plans the step itself. Its output
+must match the oracle, equal the planner-kernel path bit for bit, and leave
+the same plan words as the planners."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_hpc_gb300 as hpc
+from paged_gqa_decode_hpc_gb300 import workloads as W
+from tests.gpu_util import assert_parity, device_workload, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    hpc.load_library()
+
+
+def _cfg(hq=64, hkv=8, fp8=False):
+    return W.Config(92, "step", hq, hkv, "fp8_e4m3" if fp8 else "bf16")
+
+
+def run_step(w, d=None, num_sms=None, plan=None):
+    d = d or device_workload(w)
+    sms_all = hpc.hpc_device_sm_count()
+    num_sms = num_sms or sms_all
+    B, hq = w.q.shape[0], w.q.shape[1]
+    own = plan is None
+    if own:
+        plan = hpc.hpc_decode_plan_create(max(B, 1), sms_all, hq)
+    out = torch.full((B, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device="cuda")
+    hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, num_sms, out, lse,
+                        k_scale=w.k_scale, v_scale=w.v_scale)
+    torch.cuda.synchronize()
+    err = hpc.hpc_decode_plan_status(plan)
+    words = hpc.hpc_decode_plan_export(plan)
+    if own:
+        plan.destroy()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy(), words, err
+
+
+@pytest.mark.parametrize("lens,hq,hkv,fp8,sms", [
+    ([37, 64, 200, 1000], 8, 1, False, None),
+    ([37, 64, 200, 1000], 8, 1, False, 1),
+    ([1, 63, 64, 65, 127, 129, 700, 3001], 64, 8, False, 7),
+    ([1, 63, 64, 65, 127, 129, 700, 3001], 64, 8, True, None),
+    ([0, 5, 0, 300, 4096, 0], 16, 2, False, 3),
+    ([700, 65, 3001], 128, 16, False, None),
+])
+def test_step_parity_and_plan_words(lens, hq, hkv, fp8, sms):
+    w = W.make_workload(_cfg(hq, hkv, fp8), lengths=lens, seed=41)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w, num_sms=sms)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label=f"step {lens[:4]}")
+    n = sms or hpc.hpc_device_sm_count()
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute(lens, n))
+    # the planner-kernel path gives the same bits
+    out2, lse2 = run_cuda(w, plan="device", num_sms=n)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_step_skewed_config():
+    w = W.make_workload("skewed")
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label="step skewed")
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute(w.seq_lens.tolist(),
+                                                              hpc.hpc_device_sm_count()))
+
+
+def test_step_many_sequences_uses_the_planner_kernel():
+    lens = [(i * 37) % 150 + 1 for i in range(3500)]  # above the in-kernel limit
+    w = W.make_workload(_cfg(8, 1), lengths=lens, seed=42)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label="step 3500 seqs")
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute(lens, hpc.hpc_device_sm_count()))
+
+
+def test_step_negative_length_sets_check():
+    w = W.make_workload(_cfg(), lengths=[100, 50], seed=43)
+    d = device_workload(w)
+    d["sl"][1] = -5
+    out, lse, words, err = run_step(w, d=d)
+    assert err & hpc.HPC_DEVCHK_BAD_LENGTH
+    assert words[3] == 0 and words[5] == 0  # empty plan
+
+
+def test_step_reuses_one_plan_across_batches_and_graph_capture():
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(16, sms, 64)
+    for seed, lens in [(44, [3000, 64, 1]), (45, [512] * 16), (46, [9000])]:
+        w = W.make_workload(_cfg(), lengths=lens, seed=seed)
+        ref_out, ref_lse = oracle.decode_workload(w)
+        out, lse, words, err = run_step(w, plan=plan)
+        assert err == 0
+        assert_parity(out, lse, ref_out, ref_lse)
+    w = W.make_workload(_cfg(), lengths=[2000, 640, 7], seed=47)
+    d = device_workload(w)
+    out = torch.zeros(w.q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out, lse, stream=s)
+    torch.cuda.synchronize()
+    out.zero_(); lse.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out, lse, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert hpc.hpc_decode_plan_status(plan) == 0
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse)
+    plan.destroy()
