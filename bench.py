@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--no-prologue", action="store_true",
+                    help="skip timing the fused prologue kernel")
     ap.add_argument("--no-copy-probe", action="store_true",
                     help="skip the device-to-device copy bandwidth probe")
     ap.add_argument("--scale-lengths", type=float, default=1.0,
@@ -507,6 +509,46 @@ def run_hpc(args, ws, rank, local):
             "cores": oracle.num_cpus(), "kind": "oracle",
             "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
                       f"{int(w.seq_lens.sum())} KV tokens), mean of 3 runs, {t:.2f} s each"}
+
+    # ---- the fused prologue (QK-Norm + RoPE + KV write) for this batch's new tokens
+    if not args.no_prologue:
+        pin = W.make_prologue_inputs(w, seed=7000)
+        qi, ki, vi = pin.q_in.to(dev), pin.k_in.to(dev), pin.v_in.to(dev)
+        wq, wk = pin.w_q.to(dev), pin.w_k.to(dev)
+        q_new = torch.empty_like(qi)
+        kc2, vc2 = kc.clone(), vc.clone()
+
+        def prologue():
+            hpc.hpc_rope_norm_kv_write(qi, ki, vi, sl, bt, wq, wk, q_new, kc2, vc2, eps=pin.eps,
+                                       rope_base=pin.rope_base, k_scale=w.k_scale,
+                                       v_scale=w.v_scale, stream=stream)
+
+        def prologue_and_step():
+            prologue()
+            hpc.hpc_decode_step(q_new, kc2, vc2, bt, sl, plan, num_sms, out, lse, stream=stream,
+                                k_scale=w.k_scale, v_scale=w.v_scale)
+
+        res = {}
+        for name, fn in (("prologue_us", prologue), ("prologue_plus_step_us", prologue_and_step)):
+            for _ in range(3):
+                flush_l2()
+                fn()
+            es = [[mk(), mk()] for _ in range(max(5, min(args.steps, 20)))]
+            for a, b_ in es:
+                flush_l2()
+                a.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            res[name] = round(statistics.mean(a.elapsed_time(b_) for a, b_ in es) * 1e3, 2)
+        rows_in = B * (hq + 2 * hkv) * 128 * 2
+        rows_out = B * hq * 128 * 2 + B * 2 * hkv * 128 * (1 if fp8 else 2)
+        pbytes = rows_in + rows_out
+        res["algorithmic_bytes"] = pbytes
+        res["achieved_gbs"] = round(pbytes / (res["prologue_us"] * 1e-6) / 1e9, 1)
+        res["note"] = "latency-bound: the bytes are small; one launch of B*(H_q+2*H_kv) warps"
+        line["prologue"] = res
+        del kc2, vc2
 
     # ---- context: a plain device-to-device copy on this GPU (read + write bytes)
     if not args.no_copy_probe:

@@ -298,6 +298,37 @@ hpc_status hpc_decode_attn_noalloc(const hpc_tensor* q, const hpc_tensor* k_cach
                                    const hpc_tensor* seq_lens, int32_t num_sms, hpc_tensor* out,
                                    hpc_tensor* lse, int32_t* device_error, void* stream);
 
+/*
+ * hpc_rope_norm_kv_write -- the fused decode prologue that feeds the path
+ * ("vLLM x HPC-Ops", section "Attention Backend: Dynamic Load-Balanced
+ * Scheduling", the HpcRopeNorm paragraph: QK-Norm, RoPE, KV-cache write and,
+ * in FP8, query quantisation in one kernel). For the new token of every
+ * sequence (position pos = seq_lens[b] - 1; sequences with seq_lens <= 0 are
+ * skipped):
+ *   q' = RoPE(RMSNorm(q) * q_norm_weight), k' = RoPE(RMSNorm(k) * k_norm_weight)
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + eps) over head_dim, per head;
+ *   RoPE rotates pairs (i, i + 64) by pos * rope_base^(-2i/128);
+ * then writes q' to q_out (bf16; may alias q_in), optionally e4m3(q' / scale)
+ * to q_out_fp8 (scale in its descriptor), and k', v into the cache at slot
+ * pos % 64 of block block_table[b][pos / 64] (bf16, or e4m3(x / scale) with
+ * the cache's per-tensor scale, round to nearest even, saturating at 448).
+ *   q_in [B][H_q][128], k_in / v_in [B][H_kv][128]: device bf16, rows contiguous
+ *   seq_lens device int32 [B] (lengths including the new token)
+ *   block_table device int32 [B][max_blocks]
+ *   q_norm_weight, k_norm_weight: device bf16 or f32 [128], 16-byte aligned
+ *   k_cache, v_cache: as hpc_decode_attn (written in place)
+ *   device_error: optional device int32 receiving HPC_DEVCHK_* bits (a block
+ *   id out of range or a table too short skips that row's write)
+ * The readings where the pages are silent (RMSNorm, norm before RoPE, the
+ * rotate-half pairing) are stated above; rope_base > 1, eps >= 0.
+ */
+hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in,
+                                  const hpc_tensor* v_in, const hpc_tensor* seq_lens,
+                                  const hpc_tensor* block_table, const hpc_tensor* q_norm_weight,
+                                  const hpc_tensor* k_norm_weight, float eps, float rope_base,
+                                  hpc_tensor* q_out, hpc_tensor* q_out_fp8, hpc_tensor* k_cache,
+                                  hpc_tensor* v_cache, int32_t* device_error, void* stream);
+
 /* hpc_device_sm_count -- streaming multiprocessors of the current device. */
 hpc_status hpc_device_sm_count(int32_t* num_sms);
 

@@ -25,6 +25,7 @@ __all__ = [
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
     "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc", "hpc_decode_step",
+    "hpc_rope_norm_kv_write",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
 ]
@@ -100,6 +101,8 @@ def load_library():
             "hpc_decode_plan_set_timing_events": [P, P, P, P],
             "hpc_decode_attn_noalloc": [T, T, T, T, T, i32, T, T, P, P],
             "hpc_decode_step": [T, T, T, T, T, P, i32, T, T, P],
+            "hpc_rope_norm_kv_write": [T, T, T, T, T, T, T, ctypes.c_float, ctypes.c_float,
+                                       T, T, T, T, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -292,6 +295,25 @@ def make_tensor(t, scale: float = 1.0) -> Optional[HpcTensor]:
         d.stride[i] = t.stride(i)
     d.scale = float(scale)
     return d
+
+
+def hpc_rope_norm_kv_write(q_in, k_in, v_in, seq_lens, block_table, q_norm_weight,
+                           k_norm_weight, q_out, k_cache, v_cache, eps: float = 1e-6,
+                           rope_base: float = 10000.0, q_out_fp8=None, q_fp8_scale: float = 1.0,
+                           k_scale: float = 1.0, v_scale: float = 1.0, device_error=None,
+                           stream=None):
+    """Fused decode prologue: QK-Norm + RoPE of the new token's q and k, the
+    paged KV-cache write of k and v, and optionally an FP8 copy of q."""
+    lib = load_library()
+    d = [make_tensor(q_in), make_tensor(k_in), make_tensor(v_in), make_tensor(seq_lens),
+         make_tensor(block_table), make_tensor(q_norm_weight), make_tensor(k_norm_weight)]
+    qo, qf = make_tensor(q_out), make_tensor(q_out_fp8, q_fp8_scale)
+    kc, vc = make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
+    ref = lambda t: ctypes.byref(t) if t is not None else None
+    err = ctypes.c_void_p(device_error.data_ptr()) if device_error is not None else None
+    _check(lib.hpc_rope_norm_kv_write(*[ref(t) for t in d], ctypes.c_float(eps),
+                                      ctypes.c_float(rope_base), ref(qo), ref(qf), ref(kc),
+                                      ref(vc), err, _stream_ptr(stream)))
 
 
 def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int, out,

@@ -627,6 +627,108 @@ hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, vo
   return HPC_OK;
 }
 
+hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in,
+                                  const hpc_tensor* v_in, const hpc_tensor* seq_lens,
+                                  const hpc_tensor* block_table, const hpc_tensor* q_norm_weight,
+                                  const hpc_tensor* k_norm_weight, float eps, float rope_base,
+                                  hpc_tensor* q_out, hpc_tensor* q_out_fp8, hpc_tensor* k_cache,
+                                  hpc_tensor* v_cache, int32_t* device_error, void* stream) {
+  hpc_status st;
+  if ((st = check_tensor(q_in, "q_in", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(k_in, "k_in", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(v_in, "v_in", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(seq_lens, "seq_lens", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(block_table, "block_table", 2)) != HPC_OK) return st;
+  if ((st = check_tensor(q_norm_weight, "q_norm_weight", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(k_norm_weight, "k_norm_weight", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(q_out, "q_out", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(q_out_fp8, "q_out_fp8", 3, true)) != HPC_OK) return st;
+  if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
+  if ((st = check_tensor(v_cache, "v_cache", 4)) != HPC_OK) return st;
+  const bool has_qf = q_out_fp8 && q_out_fp8->data;
+  const int64_t B = q_in->shape[0], Hq = q_in->shape[1], Hkv = k_in->shape[1];
+  if (q_in->dtype != HPC_BF16 || k_in->dtype != HPC_BF16 || v_in->dtype != HPC_BF16 ||
+      q_out->dtype != HPC_BF16)
+    return fail(HPC_ERR_INVALID_ARG, "q_in, k_in, v_in and q_out must be bf16");
+  if (q_in->shape[2] != kHeadDim || k_in->shape[2] != kHeadDim || v_in->shape[2] != kHeadDim ||
+      k_cache->shape[3] != kHeadDim)
+    return fail(HPC_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (k_cache->shape[2] != kBlockTokens)
+    return fail(HPC_ERR_UNSUPPORTED, "KV blocks must hold 64 tokens");
+  if (k_in->shape[0] != B || v_in->shape[0] != B || v_in->shape[1] != Hkv ||
+      q_out->shape[0] != B || q_out->shape[1] != Hq || q_out->shape[2] != kHeadDim ||
+      k_cache->shape[1] != Hkv || Hkv <= 0 || Hq % Hkv != 0)
+    return fail(HPC_ERR_INVALID_ARG, "inconsistent q/k/v/out/cache shapes");
+  if (has_qf && (q_out_fp8->dtype != HPC_FP8_E4M3 || q_out_fp8->shape[0] != B ||
+                 q_out_fp8->shape[1] != Hq || q_out_fp8->shape[2] != kHeadDim ||
+                 q_out_fp8->stride[2] != 1 || q_out_fp8->stride[0] % 4 ||
+                 q_out_fp8->stride[1] % 4 || !aligned(q_out_fp8->data, 4) ||
+                 !(q_out_fp8->scale > 0.f) || !std::isfinite(q_out_fp8->scale)))
+    return fail(HPC_ERR_INVALID_ARG, "q_out_fp8 must be e4m3 [B][H_q][128] with a positive scale");
+  for (const hpc_tensor* t : {q_in, k_in, v_in, (const hpc_tensor*)q_out})
+    if (t->stride[2] != 1 || t->stride[0] % 4 || t->stride[1] % 4 || !aligned(t->data, 8))
+      return fail(HPC_ERR_INVALID_ARG, "q/k/v/out rows must be contiguous and 8-byte aligned");
+  if (seq_lens->dtype != HPC_I32 || seq_lens->shape[0] != B || (B > 1 && seq_lens->stride[0] != 1))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
+  if (block_table->dtype != HPC_I32 || block_table->shape[0] != B || block_table->stride[1] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "block_table must be int32 [B][max_blocks]");
+  for (const hpc_tensor* w : {q_norm_weight, k_norm_weight})
+    if ((w->dtype != HPC_BF16 && w->dtype != HPC_F32) || w->shape[0] != kHeadDim ||
+        w->stride[0] != 1 || !aligned(w->data, 16))
+      return fail(HPC_ERR_INVALID_ARG, "norm weights must be contiguous bf16/f32 [128], 16-B aligned");
+  if (k_cache->dtype != v_cache->dtype ||
+      (k_cache->dtype != HPC_BF16 && k_cache->dtype != HPC_FP8_E4M3))
+    return fail(HPC_ERR_INVALID_ARG, "k_cache/v_cache must both be bf16 or both fp8_e4m3");
+  const bool fp8 = k_cache->dtype == HPC_FP8_E4M3;
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i] || k_cache->stride[i] != v_cache->stride[i])
+      return fail(HPC_ERR_INVALID_ARG, "k_cache and v_cache must have the same shape and strides");
+  if (k_cache->stride[3] != 1 || k_cache->stride[0] % 4 || k_cache->stride[1] % 4 ||
+      k_cache->stride[2] % 4 || !aligned(k_cache->data, 8) || !aligned(v_cache->data, 8))
+    return fail(HPC_ERR_INVALID_ARG, "cache rows must be contiguous and 8-byte aligned");
+  if (fp8 && (!(k_cache->scale > 0.f) || !(v_cache->scale > 0.f) ||
+              !std::isfinite(k_cache->scale) || !std::isfinite(v_cache->scale)))
+    return fail(HPC_ERR_INVALID_ARG, "FP8 caches need positive finite scales");
+  if (!(eps >= 0.f) || !(rope_base > 1.f) || !std::isfinite(rope_base))
+    return fail(HPC_ERR_INVALID_ARG, "eps must be >= 0 and rope_base > 1");
+  if (B == 0) return HPC_OK;
+  PrologueParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q_in = (const __nv_bfloat16*)q_in->data; p.qi_sb = q_in->stride[0]; p.qi_sh = q_in->stride[1];
+  p.k_in = (const __nv_bfloat16*)k_in->data; p.ki_sb = k_in->stride[0]; p.ki_sh = k_in->stride[1];
+  p.v_in = (const __nv_bfloat16*)v_in->data; p.vi_sb = v_in->stride[0]; p.vi_sh = v_in->stride[1];
+  p.seq_lens = (const int32_t*)seq_lens->data;
+  p.block_table = (const int32_t*)block_table->data;
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = (int32_t)block_table->shape[1];
+  p.wq = q_norm_weight->data; p.wq_dtype = q_norm_weight->dtype;
+  p.wk = k_norm_weight->data; p.wk_dtype = k_norm_weight->dtype;
+  p.eps = eps;
+  p.log2_base = std::log2((double)rope_base);
+  p.q_out = (__nv_bfloat16*)q_out->data; p.qo_sb = q_out->stride[0]; p.qo_sh = q_out->stride[1];
+  if (has_qf) {
+    p.q_fp8 = (uint8_t*)q_out_fp8->data;
+    p.qf_sb = q_out_fp8->stride[0];
+    p.qf_sh = q_out_fp8->stride[1];
+    p.q_fp8_scale = q_out_fp8->scale;
+  }
+  p.k_cache = k_cache->data;
+  p.v_cache = v_cache->data;
+  p.c_sblk = k_cache->stride[0]; p.c_shead = k_cache->stride[1]; p.c_sslot = k_cache->stride[2];
+  p.cache_fp8 = fp8;
+  p.k_scale = fp8 ? k_cache->scale : 1.f;
+  p.v_scale = fp8 ? v_cache->scale : 1.f;
+  p.num_blocks = (int32_t)std::min<int64_t>(k_cache->shape[0], INT32_MAX);
+  p.num_seqs = (int32_t)B;
+  p.num_q_heads = (int32_t)Hq;
+  p.num_kv_heads = (int32_t)Hkv;
+  p.err = device_error;
+  cudaError_t e = launch_prologue(p, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(HPC_ERR_CUDA, std::string("prologue launch: ") + cudaGetErrorString(e));
+  return HPC_OK;
+}
+
 hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
                            const hpc_tensor* v_cache, const hpc_tensor* block_table,
                            const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,

@@ -105,6 +105,38 @@ struct MergeParams {
   const float* ws_l;
 };
 
+// Parameter block of the fused prologue kernel (prologue_kernel.cu).
+struct PrologueParams {
+  const __nv_bfloat16* q_in;
+  int64_t qi_sb, qi_sh;
+  const __nv_bfloat16* k_in;
+  int64_t ki_sb, ki_sh;
+  const __nv_bfloat16* v_in;
+  int64_t vi_sb, vi_sh;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int64_t bt_sb;
+  int32_t max_blocks;
+  const void* wq;
+  const void* wk;
+  int32_t wq_dtype, wk_dtype;  // HPC_BF16 or HPC_F32
+  float eps;
+  double log2_base;
+  __nv_bfloat16* q_out;
+  int64_t qo_sb, qo_sh;
+  uint8_t* q_fp8;  // may be null
+  int64_t qf_sb, qf_sh;
+  float q_fp8_scale;
+  void* k_cache;
+  void* v_cache;
+  int64_t c_sblk, c_shead, c_sslot;  // element strides (same for K and V)
+  int32_t cache_fp8;
+  float k_scale, v_scale;
+  int32_t num_blocks, num_seqs, num_q_heads, num_kv_heads;
+  int32_t* err;  // may be null
+};
+cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
+
 // Host planners (plan_host.cu). Fill `words` (canonical layout sized by the
 // returned length) or report an error message.
 hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,

@@ -168,3 +168,28 @@ def make_workload(cfg: Config | str, lengths: Optional[List[int]] = None,
         ks = vs = 1.0
     return Workload(cfg.name, torch.tensor(lens, dtype=torch.int32), bt, q, k, v,
                     ks, vs, cfg.kv_dtype, 1.0 / math.sqrt(HEAD_DIM), hq, hkv)
+
+
+@dataclasses.dataclass
+class PrologueInputs:
+    """The new token's projections for the fused prologue (host tensors)."""
+    q_in: torch.Tensor      # bf16 [B][H_q][D]
+    k_in: torch.Tensor      # bf16 [B][H_kv][D]
+    v_in: torch.Tensor      # bf16 [B][H_kv][D]
+    w_q: torch.Tensor       # bf16 [D] RMSNorm weight of q
+    w_k: torch.Tensor       # bf16 [D]
+    eps: float
+    rope_base: float
+
+
+def make_prologue_inputs(w: Workload, seed: int, eps: float = 1e-6,
+                         rope_base: float = 10000.0) -> PrologueInputs:
+    """Seeded N(0,1) q/k/v rows and weights 1 + 0.1 N(0,1) (all bf16)."""
+    gen = torch.Generator().manual_seed(seed)
+    B, hq, hkv = w.num_seqs, w.num_q_heads, w.num_kv_heads
+    q = torch.randn(B, hq, HEAD_DIM, generator=gen).to(torch.bfloat16)
+    k = torch.randn(B, hkv, HEAD_DIM, generator=gen).to(torch.bfloat16)
+    v = torch.randn(B, hkv, HEAD_DIM, generator=gen).to(torch.bfloat16)
+    wq = (1 + 0.1 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16)
+    wk = (1 + 0.1 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16)
+    return PrologueInputs(q, k, v, wq, wk, eps, rope_base)
