@@ -704,7 +704,14 @@ hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in
   p.wq = q_norm_weight->data; p.wq_dtype = q_norm_weight->dtype;
   p.wk = k_norm_weight->data; p.wk_dtype = k_norm_weight->dtype;
   p.eps = eps;
-  p.log2_base = std::log2((double)rope_base);
+  for (int i = 0; i < kHeadDim / 2; ++i) {
+    const double f = std::pow((double)rope_base, -2.0 * i / kHeadDim);
+    p.inv_freq_hi[i] = (float)f;
+    p.inv_freq_lo[i] = (float)(f - (double)p.inv_freq_hi[i]);
+  }
+  const double two_pi = 2.0 * 3.14159265358979323846;
+  p.two_pi_hi = (float)two_pi;
+  p.two_pi_lo = (float)(two_pi - (double)p.two_pi_hi);
   p.q_out = (__nv_bfloat16*)q_out->data; p.qo_sb = q_out->stride[0]; p.qo_sh = q_out->stride[1];
   if (has_qf) {
     p.q_fp8 = (uint8_t*)q_out_fp8->data;

@@ -121,7 +121,10 @@ struct PrologueParams {
   const void* wk;
   int32_t wq_dtype, wk_dtype;  // HPC_BF16 or HPC_F32
   float eps;
-  double log2_base;
+  // RoPE inverse frequencies base^(-2i/128) as float-float pairs, and 2*pi
+  // split the same way (both formed on the host in double precision)
+  float inv_freq_hi[64], inv_freq_lo[64];
+  float two_pi_hi, two_pi_lo;
   __nv_bfloat16* q_out;
   int64_t qo_sb, qo_sh;
   uint8_t* q_fp8;  // may be null

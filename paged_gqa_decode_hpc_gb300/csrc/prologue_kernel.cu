@@ -8,8 +8,11 @@
 //
 // One warp per row (a query head, a key head or a value head of one
 // sequence); lane l holds elements [4l, 4l + 4), so the RoPE partner
-// (i <-> i + 64) is lane l ^ 16. Angles are formed in double precision
-// (positions reach 2^18 and beyond), the rest in fp32.
+// (i <-> i + 64) is lane l ^ 16. Positions reach 2^18 and beyond, where an
+// fp32 product pos * f is off by ~1e-2 rad; the angle is therefore carried as
+// a float-float sum (exact FMA product terms, host-made double-precision
+// frequencies split in two floats) and reduced modulo 2*pi before sincosf.
+// Everything runs in fp32 (GB300's fp64 rate is a small fraction of it).
 #include <cuda_bf16.h>
 
 #include "hpc_internal.h"
@@ -79,14 +82,19 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) prologue_kernel(const Prolog
                                  __shfl_xor_sync(0xffffffffu, x.w, 16));
     const float sgn = lane < 16 ? -1.f : 1.f;
     float c[4], s[4];
+    const float fpos = (float)pos;  // exact below 2^24
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = 4 * (lane & 15) + j;
-      const double ang = (double)pos * exp2(-(2.0 * i / kHeadDim) * p.log2_base);
-      double sd, cd;
-      sincos(ang, &sd, &cd);
-      c[j] = (float)cd;
-      s[j] = (float)sd;
+      // angle = pos * f with f = f_hi + f_lo: pos * f_hi exactly as a_hi + a_err
+      const float a_hi = fpos * p.inv_freq_hi[i];
+      const float a_err = fmaf(fpos, p.inv_freq_hi[i], -a_hi);
+      const float a_lo = fmaf(fpos, p.inv_freq_lo[i], a_err);
+      // reduce modulo 2*pi (= two_pi_hi + two_pi_lo) into [-pi, pi]
+      const float k = rintf(a_hi * (1.0f / p.two_pi_hi));
+      float r = fmaf(-k, p.two_pi_hi, a_hi);
+      r = fmaf(-k, p.two_pi_lo, r) + a_lo;
+      sincosf(r, &s[j], &c[j]);
     }
     x = make_float4(x.x * c[0] + sgn * y.x * s[0], x.y * c[1] + sgn * y.y * s[1],
                     x.z * c[2] + sgn * y.z * s[2], x.w * c[3] + sgn * y.w * s[3]);
