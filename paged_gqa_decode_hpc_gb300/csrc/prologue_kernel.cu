@@ -11,7 +11,7 @@
 // (i <-> i + 64) is lane l ^ 16. Positions reach 2^18 and beyond, where an
 // fp32 product pos * f is off by ~1e-2 rad; the angle is therefore carried as
 // a float-float sum (exact FMA product terms, host-made double-precision
-// frequencies split in two floats) and reduced modulo 2*pi before sincosf.
+// frequencies split in two floats) and reduced modulo 2*pi before the sine.
 // Everything runs in fp32 (GB300's fp64 rate is a small fraction of it).
 #include <cuda_bf16.h>
 
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) prologue_kernel(const Prolog
       const float k = rintf(a_hi * (1.0f / p.two_pi_hi));
       float r = fmaf(-k, p.two_pi_hi, a_hi);
       r = fmaf(-k, p.two_pi_lo, r) + a_lo;
-      sincosf(r, &s[j], &c[j]);
+      __sincosf(r, &s[j], &c[j]);  // |r| <= pi: absolute error ~5e-7
     }
     x = make_float4(x.x * c[0] + sgn * y.x * s[0], x.y * c[1] + sgn * y.y * s[1],
                     x.z * c[2] + sgn * y.z * s[2], x.w * c[3] + sgn * y.w * s[3]);
