@@ -140,3 +140,28 @@ def decode_workload(w, num_threads: int = 0, lib=None):
                         num_kv_heads=w.num_kv_heads, softmax_scale=w.softmax_scale,
                         kv_is_fp8=(w.kv_dtype == "fp8_e4m3"), k_scale=w.k_scale,
                         v_scale=w.v_scale, num_threads=num_threads, lib=lib)
+
+
+def paged_decode_multi(q, k_cache, v_cache, block_table, seq_lens, *, num_kv_heads: int,
+                       softmax_scale: float, kv_is_fp8: bool = False, k_scale: float = 1.0,
+                       v_scale: float = 1.0, num_threads: int = 0, lib=None):
+    """Decode of q_len new query tokens per sequence (multi-token / draft
+    verification), by its definition: the q_len tokens are the last q_len
+    positions of the sequence, and token t attends causally to the positions
+    before L - q_len + 1 + t. Each (sequence, token) is therefore a plain decode
+    of that length over the same block table.
+
+    q: bf16 [B][q_len][H_q][D]. Returns (out [B][q_len][H_q][D], lse [B][q_len][H_q]).
+    """
+    import torch
+    qt = q if hasattr(q, "shape") else np.asarray(q)
+    B, T = int(qt.shape[0]), int(qt.shape[1])
+    lens = _as_np(seq_lens, np.int32)
+    vlen = np.array([max(0, int(lens[b]) - T + 1 + t) for b in range(B) for t in range(T)],
+                    dtype=np.int32)
+    bt = np.repeat(_as_np(block_table, np.int32), T, axis=0)
+    qv = qt.reshape(B * T, qt.shape[2], qt.shape[3])
+    out, lse = paged_decode(qv, k_cache, v_cache, bt, vlen, num_kv_heads=num_kv_heads,
+                            softmax_scale=softmax_scale, kv_is_fp8=kv_is_fp8, k_scale=k_scale,
+                            v_scale=v_scale, num_threads=num_threads, lib=lib)
+    return out.reshape(B, T, qt.shape[2], -1), lse.reshape(B, T, -1)

@@ -311,10 +311,11 @@ __device__ __forceinline__ int acc_d(int dm, int r, int g) {
 
 // Q of one (sequence, kv head) as mma B fragments (B[k = d][n = q head]).
 template <bool FP8>
-__device__ __forceinline__ float load_q(const AttnParams& p, int b, int h, int lane,
+__device__ __forceinline__ float load_q(const AttnParams& p, int b, int t, int h, int lane,
                                         uint32_t (&qf)[8][2]) {
   const int g = lane >> 2, c = lane & 3;
-  const __nv_bfloat16* qrow = p.q + (int64_t)b * p.q_sb + (int64_t)(h * kGroup + g) * p.q_sh;
+  const __nv_bfloat16* qrow = p.q + (int64_t)b * p.q_sb + (int64_t)t * p.q_st +
+                              (int64_t)(h * kGroup + g) * p.q_sh;
   if constexpr (!FP8) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
@@ -485,7 +486,8 @@ __device__ __forceinline__ void compute_unit(uint32_t kbase, uint32_t vbase,
 
 // Final output (whole sequence in this CTA) or a partial state.
 template <bool FP8>
-__device__ __forceinline__ void write_result(const AttnParams& p, bool whole, int b, int h, int seg,
+__device__ __forceinline__ void write_result(const AttnParams& p, bool whole, int b, int t, int h,
+                                             int seg,
                                              const float (&m)[2], const float (&l)[2],
                                              const float (&acc)[8][4], int lane) {
   const int g = lane >> 2, c = lane & 3;
@@ -494,7 +496,7 @@ __device__ __forceinline__ void write_result(const AttnParams& p, bool whole, in
     for (int e = 0; e < 2; ++e) {
       const int j = h * kGroup + 2 * c + e;
       const float inv = l[e] > 0.f ? p.v_scale / l[e] : 0.f;
-      __nv_bfloat16* orow = p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh;
+      __nv_bfloat16* orow = p.out + (int64_t)b * p.o_sb + (int64_t)t * p.o_st + (int64_t)j * p.o_sh;
       if constexpr (FP8) {
 #pragma unroll
         for (int dm = 0; dm < 8; ++dm)
@@ -508,14 +510,17 @@ __device__ __forceinline__ void write_result(const AttnParams& p, bool whole, in
         }
       }
       if (p.lse && g == 0)
-        p.lse[(int64_t)b * p.l_sb + (int64_t)j * p.l_sh] =
+        p.lse[(int64_t)b * p.l_sb + (int64_t)t * p.l_st + (int64_t)j * p.l_sh] =
             l[e] > 0.f ? (m[e] + __log2f(l[e])) * kLn2 : -INFINITY;
     }
   } else {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int j = h * kGroup + 2 * c + e;
-      float* o = p.ws_o + ((int64_t)seg * p.num_q_heads + j) * kHeadDim;
+      // partial rows are indexed by (segment, query token, query head)
+      const int64_t hv = (int64_t)p.q_len * p.num_q_heads;
+      const int64_t jv = (int64_t)t * p.num_q_heads + j;
+      float* o = p.ws_o + ((int64_t)seg * hv + jv) * kHeadDim;
 #pragma unroll
       for (int dm = 0; dm < 8; ++dm) {
         if constexpr (FP8) {
@@ -527,8 +532,8 @@ __device__ __forceinline__ void write_result(const AttnParams& p, bool whole, in
         }
       }
       if (g == 0) {
-        p.ws_m[(int64_t)seg * p.num_q_heads + j] = m[e];
-        p.ws_l[(int64_t)seg * p.num_q_heads + j] = l[e];
+        p.ws_m[(int64_t)seg * hv + jv] = m[e];
+        p.ws_l[(int64_t)seg * hv + jv] = l[e];
       }
     }
   }
@@ -557,7 +562,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, p.q_len);  // one consumer warp per query token
     }
     *abort_flag = 0;
     for (int s = 0; s < STAGES; ++s)
@@ -671,9 +676,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     h_begin = 0;
     h_count = p.num_kv_heads;
   }
-  const int hpass = h_count < NC ? h_count : NC;  // kv heads processed together
-  const int npass = h_count / hpass;
-  const int wph = NC / hpass;                     // consumer warps per kv head
+  // KV heads processed together per pass; each (tile, head) unit is read by
+  // q_len consumer warps (one per query token), and tph warps per (head,
+  // token) split the tiles when warps are left over.
+  const WarpLayout wl = warp_layout(h_count, p.q_len, NC);
+  const int hpass = wl.hpass, npass = wl.npass, tph = wl.tph;
   __syncthreads();
 
   if (warp == NC) {
@@ -753,8 +760,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 
   // -------------------------------------------------------------- consumers
   float* comb = reinterpret_cast<float*>(smem + Cfg::kCombOff);
-  const int hl = warp % hpass;      // kv head (within the pass) of this warp
-  const int tphase = warp / hpass;  // this warp takes tiles i = tphase (mod wph)
+  const int hl = warp % hpass;                     // kv head (within the pass)
+  const int tok = (warp / hpass) % p.q_len;        // query token of this warp
+  const int tphase = (warp / hpass) / p.q_len;     // tiles i = tphase (mod tph)
+  const bool active = tphase < tph;                // idle when warps are left over
   const int c = lane & 3;
   uint32_t gbase = 0;
   bool dead = false;
@@ -775,11 +784,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       float acc[8][4];
 #pragma unroll
       for (int dm = 0; dm < 8; ++dm) acc[dm][0] = acc[dm][1] = acc[dm][2] = acc[dm][3] = 0.f;
-      if (tphase < n) {
+      // causal limit of this warp's query token: the q_len new tokens are the
+      // last q_len positions of the sequence
+      const int len_t = len - (p.q_len - 1 - tok);
+      if (active && tphase < n) {
         uint32_t qf[8][2];
-        const float qinv = load_q<FP8>(p, b, h, lane, qf);
+        const float qinv = load_q<FP8>(p, b, tok, h, lane, qf);
         const float sl2 = p.score_scale_log2 * qinv;
-        for (int i = tphase; i < n; i += wph) {
+        for (int i = tphase; i < n; i += tph) {
           const uint32_t gu = gbase + (uint32_t)(i * hpass + hl);
           const uint32_t slot = gu % STAGES;
           if (dead) continue;
@@ -791,7 +803,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             dead = true;
             continue;
           }
-          const int valid = len - (tb + i) * kBlockTokens;
+          const int valid = len_t - (tb + i) * kBlockTokens;
           if (valid > 0) {
             const uint32_t kb = smem_base + slot * kStage;
             compute_unit<FP8>(kb, kb + kTile, qf, valid, sl2, m, l, acc, lane);
@@ -807,10 +819,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
         l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
       }
-      if (!COMBINE || wph == 1) {
-        if (!dead) write_result<FP8>(p, whole, b, h, seg, m, l, acc, lane);
+      if (!COMBINE || tph == 1) {
+        if (!dead && active) write_result<FP8>(p, whole, b, tok, h, seg, m, l, acc, lane);
       } else {
-        if (tphase > 0) {
+        // warps of one (head, token): hl + hpass * (tok + q_len * k), k < tph
+        const int wstep = hpass * p.q_len;
+        if (active && tphase > 0) {
           float* cw = comb + (warp * 32 + lane) * kCombineFloats;
 #pragma unroll
           for (int dm = 0; dm < 8; ++dm)
@@ -819,11 +833,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           *reinterpret_cast<float4*>(cw + 32) = make_float4(m[0], m[1], l[0], l[1]);
         }
         named_bar_sync(1, NC * 32);
-        if (tphase == 0) {
+        if (active && tphase == 0) {
           float M0 = m[0], M1 = m[1];
-          for (int k = 1; k < wph; ++k) {
+          for (int k = 1; k < tph; ++k) {
             const float4 ml =
-                *reinterpret_cast<const float4*>(comb + ((warp + k * hpass) * 32 + lane) *
+                *reinterpret_cast<const float4*>(comb + ((warp + k * wstep) * 32 + lane) *
                                                             kCombineFloats + 32);
             M0 = fmaxf(M0, ml.x);
             M1 = fmaxf(M1, ml.y);
@@ -839,8 +853,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             acc[dm][2] *= f0;
             acc[dm][3] *= f1;
           }
-          for (int k = 1; k < wph; ++k) {
-            const float* cw = comb + ((warp + k * hpass) * 32 + lane) * kCombineFloats;
+          for (int k = 1; k < tph; ++k) {
+            const float* cw = comb + ((warp + k * wstep) * 32 + lane) * kCombineFloats;
             const float4 ml = *reinterpret_cast<const float4*>(cw + 32);
             const float k0 = ml.x == -INFINITY ? 0.f : ex2(ml.x - M0);
             const float k1 = ml.y == -INFINITY ? 0.f : ex2(ml.y - M1);
@@ -857,7 +871,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           }
           m[0] = M0;
           m[1] = M1;
-          if (!*abort_flag) write_result<FP8>(p, whole, b, h, seg, m, l, acc, lane);
+          if (!*abort_flag) write_result<FP8>(p, whole, b, tok, h, seg, m, l, acc, lane);
         }
         named_bar_sync(1, NC * 32);
       }
@@ -897,7 +911,7 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              bool fp8, int gx, int gy, cudaStream_t stream) {
   const int hc = p.static_mode ? 1 : p.num_kv_heads;
-  const bool combine = hc < 8;
+  const bool combine = warp_layout(hc, p.q_len, 8).tph > 1;
   if (fp8) {
     return combine ? launch_cfg<true, 10, 8, true>(p, tk, tv, gx, gy, stream)
                    : launch_cfg<true, 12, 8, false>(p, tk, tv, gx, gy, stream);

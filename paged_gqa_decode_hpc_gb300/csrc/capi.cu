@@ -415,17 +415,26 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale, void* stream,
                      int32_t fused_num_sms) {
   hpc_status st;
-  if ((st = check_tensor(q, "q", 3)) != HPC_OK) return st;
+  // q/out are [B][H_q][128] (one query token per sequence) or
+  // [B][q_len][H_q][128] (q_len new tokens; lse then [B][q_len][H_q]).
+  const int qnd = q ? q->ndim : 0;
+  if (qnd != 3 && qnd != 4) return fail(HPC_ERR_INVALID_ARG, "q must be [B][H_q][128] or [B][q_len][H_q][128]");
+  if ((st = check_tensor(q, "q", qnd)) != HPC_OK) return st;
   if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
   if ((st = check_tensor(v_cache, "v_cache", 4)) != HPC_OK) return st;
   if ((st = check_tensor(block_table, "block_table", 2)) != HPC_OK) return st;
   if ((st = check_tensor(seq_lens, "seq_lens", 1)) != HPC_OK) return st;
-  if ((st = check_tensor(out, "out", 3)) != HPC_OK) return st;
-  if ((st = check_tensor(lse, "lse", 2, true)) != HPC_OK) return st;
+  if ((st = check_tensor(out, "out", qnd)) != HPC_OK) return st;
+  if ((st = check_tensor(lse, "lse", qnd - 1, true)) != HPC_OK) return st;
   if (!plan) return fail(HPC_ERR_INVALID_ARG, "plan is null");
   const bool has_lse = lse && lse->data;
-
-  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const bool multi = qnd == 4;
+  const int64_t B = q->shape[0], T = multi ? q->shape[1] : 1;
+  const int64_t Hq = q->shape[qnd - 2], D = q->shape[qnd - 1];
+  const int64_t q_st = multi ? q->stride[1] : 0, q_sh = q->stride[qnd - 2];
+  const int64_t o_st = multi ? out->stride[1] : 0, o_sh = out->stride[qnd - 2];
+  const int64_t l_st = (has_lse && multi) ? lse->stride[1] : 0;
+  const int64_t l_sh = has_lse ? lse->stride[qnd - 2] : 0;
   const int64_t NB = k_cache->shape[0], Hkv = k_cache->shape[1];
   if (q->dtype != HPC_BF16) return fail(HPC_ERR_INVALID_ARG, "q must be bf16");
   if (out->dtype != HPC_BF16) return fail(HPC_ERR_INVALID_ARG, "out must be bf16");
@@ -444,17 +453,24 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     return fail(HPC_ERR_UNSUPPORTED, "num_q_heads must be 8 * num_kv_heads");
   if (!(Hkv == 1 || Hkv == 2 || Hkv == 4 || (Hkv % 8 == 0 && Hkv <= 64)))
     return fail(HPC_ERR_UNSUPPORTED, "num_kv_heads must be 1, 2, 4, 8, 16, 32 or 64");
-  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D)
-    return fail(HPC_ERR_INVALID_ARG, "out must have q's shape");
-  if (has_lse && (lse->dtype != HPC_F32 || lse->shape[0] != B || lse->shape[1] != Hq))
-    return fail(HPC_ERR_INVALID_ARG, "lse must be f32 [B][H_q]");
+  if (T < 1 || T > kMaxQueryTokens)
+    return fail(HPC_ERR_UNSUPPORTED, "q_len must be between 1 and 8");
+  for (int i = 0; i < qnd; ++i)
+    if (out->shape[i] != q->shape[i])
+      return fail(HPC_ERR_INVALID_ARG, "out must have q's shape");
+  if (has_lse) {
+    if (lse->dtype != HPC_F32) return fail(HPC_ERR_INVALID_ARG, "lse must be f32");
+    for (int i = 0; i < qnd - 1; ++i)
+      if (lse->shape[i] != q->shape[i])
+        return fail(HPC_ERR_INVALID_ARG, "lse must be [B][H_q] or [B][q_len][H_q]");
+  }
   if (block_table->dtype != HPC_I32 || block_table->shape[0] != B || block_table->stride[1] != 1)
     return fail(HPC_ERR_INVALID_ARG, "block_table must be int32 [B][max_blocks], row-contiguous");
   if (seq_lens->dtype != HPC_I32 || seq_lens->shape[0] != B || (B > 1 && seq_lens->stride[0] != 1))
     return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
-  if (q->stride[2] != 1 || out->stride[2] != 1 || k_cache->stride[3] != 1)
+  if (q->stride[qnd - 1] != 1 || out->stride[qnd - 1] != 1 || k_cache->stride[3] != 1)
     return fail(HPC_ERR_INVALID_ARG, "innermost stride of q, out and the caches must be 1");
-  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+  if (q->stride[0] % 8 || q_st % 8 || q_sh % 8 || out->stride[0] % 8 || o_st % 8 || o_sh % 8 ||
       !aligned(q->data, 16) || !aligned(out->data, 16))
     return fail(HPC_ERR_INVALID_ARG, "q/out must be 16-byte aligned with strides of 8 elements");
   const int64_t e = fp8 ? 1 : 2;
@@ -495,7 +511,7 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
   } else {
     gx = plan->host_num_parts >= 0 ? plan->host_num_parts : plan->num_sms;
   }
-  st = ensure_workspace(plan, Hq, plan->h_pinned == nullptr);
+  st = ensure_workspace(plan, T * Hq, plan->h_pinned == nullptr);
   if (st != HPC_OK) return st;
 
   const PlanLayout& L = plan->layout;
@@ -509,13 +525,17 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     std::memset(&p, 0, sizeof p);
     p.q = (const __nv_bfloat16*)q->data;
     p.q_sb = q->stride[0];
-    p.q_sh = q->stride[1];
+    p.q_st = q_st;
+    p.q_sh = q_sh;
     p.out = (__nv_bfloat16*)out->data;
     p.o_sb = out->stride[0];
-    p.o_sh = out->stride[1];
+    p.o_st = o_st;
+    p.o_sh = o_sh;
     p.lse = has_lse ? (float*)lse->data : nullptr;
     p.l_sb = has_lse ? lse->stride[0] : 0;
-    p.l_sh = has_lse ? lse->stride[1] : 0;
+    p.l_st = l_st;
+    p.l_sh = l_sh;
+    p.q_len = (int32_t)T;
     p.block_table = (const int32_t*)block_table->data;
     p.bt_sb = block_table->stride[0];
     p.max_blocks = (int32_t)block_table->shape[1];
@@ -539,8 +559,8 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     p.v_scale = fp8 ? v_cache->scale : 1.0f;
     const int64_t cs = std::max<int64_t>(L.cap_segs, 1);
     p.ws_o = plan->d_ws;
-    p.ws_m = plan->d_ws + cs * Hq * kHeadDim;
-    p.ws_l = p.ws_m + cs * Hq;
+    p.ws_m = plan->d_ws + cs * T * Hq * kHeadDim;
+    p.ws_l = p.ws_m + cs * T * Hq;
     p.err = plan->d_err;
     p.timeout_ns = wait_limit_ns();
     if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
@@ -553,10 +573,13 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
   std::memset(&mp, 0, sizeof mp);
   mp.out = (__nv_bfloat16*)out->data;
   mp.o_sb = out->stride[0];
-  mp.o_sh = out->stride[1];
+  mp.o_st = o_st;
+  mp.o_sh = o_sh;
   mp.lse = has_lse ? (float*)lse->data : nullptr;
   mp.l_sb = has_lse ? lse->stride[0] : 0;
-  mp.l_sh = has_lse ? lse->stride[1] : 0;
+  mp.l_st = l_st;
+  mp.l_sh = l_sh;
+  mp.q_len = (int32_t)T;
   mp.plan = plan->d_words;
   mp.seq_off = (int32_t)L.seq_off();
   mp.seg_off = (int32_t)L.seg_off();
@@ -564,8 +587,8 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
   mp.num_q_heads = (int32_t)Hq;
   const int64_t cs = std::max<int64_t>(L.cap_segs, 1);
   mp.ws_o = plan->d_ws;
-  mp.ws_m = plan->d_ws + cs * Hq * kHeadDim;
-  mp.ws_l = mp.ws_m + cs * Hq;
+  mp.ws_m = plan->d_ws + cs * T * Hq * kHeadDim;
+  mp.ws_l = mp.ws_m + cs * T * Hq;
   cudaError_t ce = launch_merge(mp, (int32_t)Hkv, s);
   if (ce != cudaSuccess)
     return fail(HPC_ERR_CUDA, std::string("merge launch: ") + cudaGetErrorString(ce));
@@ -593,8 +616,8 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
                            hpc_tensor* out, hpc_tensor* lse, void* stream) {
   if (!plan || plan->kind != HPC_PLAN_DYNAMIC || !plan->h_pinned)
     return fail(HPC_ERR_INVALID_ARG, "plan must come from hpc_decode_plan_create");
-  if (!q || !q->data || q->ndim != 3)
-    return fail(HPC_ERR_INVALID_ARG, "q must be a 3-D tensor [B][H_q][128]");
+  if (!q || !q->data || (q->ndim != 3 && q->ndim != 4))
+    return fail(HPC_ERR_INVALID_ARG, "q must be [B][H_q][128] or [B][q_len][H_q][128]");
   if (!seq_lens || !seq_lens->data || seq_lens->ndim != 1 || seq_lens->dtype != HPC_I32 ||
       seq_lens->shape[0] != q->shape[0] || (q->shape[0] > 1 && seq_lens->stride[0] != 1))
     return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous device int32 [B]");

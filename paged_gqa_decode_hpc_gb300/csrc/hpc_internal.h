@@ -65,11 +65,12 @@ namespace hpc {
 // Kernel parameter block of the attention kernel (passed by value).
 struct AttnParams {
   const __nv_bfloat16* q;
-  int64_t q_sb, q_sh;           // strides (elements) of q over b, head
+  int64_t q_sb, q_st, q_sh;     // strides (elements) of q over b, query token, head
   __nv_bfloat16* out;
-  int64_t o_sb, o_sh;
+  int64_t o_sb, o_st, o_sh;
   float* lse;                   // may be null
-  int64_t l_sb, l_sh;
+  int64_t l_sb, l_st, l_sh;
+  int32_t q_len;                // query tokens per sequence (1 = plain decode)
   const int32_t* block_table;
   int64_t bt_sb;
   int32_t max_blocks;
@@ -94,12 +95,13 @@ struct AttnParams {
 
 struct MergeParams {
   __nv_bfloat16* out;
-  int64_t o_sb, o_sh;
+  int64_t o_sb, o_st, o_sh;
   float* lse;
-  int64_t l_sb, l_sh;
+  int64_t l_sb, l_st, l_sh;
+  int32_t q_len;
   const int32_t* plan;
   int32_t seq_off, seg_off;
-  int32_t num_seqs, num_q_heads;
+  int32_t num_seqs, num_q_heads;  // num_q_heads per query token
   const float* ws_o;
   const float* ws_m;
   const float* ws_l;
@@ -155,6 +157,25 @@ cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_
                                cudaStream_t stream);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              bool fp8, int grid_x, int grid_y, cudaStream_t stream);
+// Query tokens per sequence the attention kernel supports (one consumer warp
+// per token and KV head).
+constexpr int32_t kMaxQueryTokens = 8;
+// Consumer-warp layout shared by the kernel and its launcher: KV heads taken
+// together per pass, and tile phases (warps splitting one head's tiles).
+struct WarpLayout {
+  int hpass, npass, tph;
+};
+__host__ __device__ inline WarpLayout warp_layout(int h_count, int q_len, int nc) {
+  int hpass = nc / q_len;
+  if (hpass < 1) hpass = 1;
+  if (hpass > h_count) hpass = h_count;
+  while (h_count % hpass) --hpass;
+  WarpLayout wl;
+  wl.hpass = hpass;
+  wl.npass = h_count / hpass;
+  wl.tph = (nc / hpass) / q_len;
+  return wl;
+}
 // Largest batch the attention kernel can plan by itself (prefix arrays in
 // shared memory next to the K/V ring).
 constexpr int32_t kFusedPlanMaxSeqs = 3072;

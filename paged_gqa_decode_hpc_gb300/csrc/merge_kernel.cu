@@ -43,13 +43,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   __shared__ float4 s_o[kMergeWarps][32];
   __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
   griddep_wait();  // partials come from the attention kernel
-  const int b = blockIdx.x, j = blockIdx.y;
+  // blockIdx.y = t * H_q + j: query token t, query head j
+  const int b = blockIdx.x, jv = blockIdx.y;
+  const int t = jv / p.num_q_heads, j = jv % p.num_q_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s0 = p.plan[p.seq_off + b], s1 = p.plan[p.seq_off + b + 1];
   const int ns = s1 - s0;
   if (ns == 1) return;  // written by the attention kernel
-  __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh + 4 * lane;
-  float* lse = p.lse ? p.lse + (int64_t)b * p.l_sb + (int64_t)j * p.l_sh : nullptr;
+  __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)t * p.o_st + (int64_t)j * p.o_sh +
+                     4 * lane;
+  float* lse = p.lse ? p.lse + (int64_t)b * p.l_sb + (int64_t)t * p.l_st + (int64_t)j * p.l_sh
+                     : nullptr;
   if (ns == 0) {
     if (warp == 0) {
       *reinterpret_cast<uint2*>(o) = make_uint2(0u, 0u);
@@ -57,8 +61,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     }
     return;
   }
-  const int64_t hq = p.num_q_heads;
-  const float* obase = p.ws_o + (int64_t)j * kHeadDim + 4 * lane;
+  const int64_t hq = (int64_t)p.q_len * p.num_q_heads;  // partial rows per segment
+  const float* obase = p.ws_o + (int64_t)jv * kHeadDim + 4 * lane;
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // this warp's partials: s0 + warp + kMergeWarps * t, t = 0, 1, ...
@@ -68,8 +72,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     const int64_t my_s = s0 + warp + (int64_t)kMergeWarps * (r0 + lane);
     float mk = -INFINITY, lk = 0.f;
     if (lane < cnt) {
-      mk = p.ws_m[my_s * hq + j];
-      lk = p.ws_l[my_s * hq + j];
+      mk = p.ws_m[my_s * hq + jv];
+      lk = p.ws_l[my_s * hq + jv];
     }
     const float Mn = fmaxf(M, warp_max(mk));
     if (Mn == -INFINITY) continue;  // only empty partials so far
@@ -104,19 +108,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, s_m[w]);
   float Lt = 0.f;
-  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
   if (Mt != -INFINITY) {
 #pragma unroll
     for (int w = 0; w < kMergeWarps; ++w) {
       const float f = s_m[w] == -INFINITY ? 0.f : ptx_ex2(s_m[w] - Mt);
       Lt += s_l[w] * f;
-      t.x += s_o[w][lane].x * f; t.y += s_o[w][lane].y * f;
-      t.z += s_o[w][lane].z * f; t.w += s_o[w][lane].w * f;
+      tot.x += s_o[w][lane].x * f; tot.y += s_o[w][lane].y * f;
+      tot.z += s_o[w][lane].z * f; tot.w += s_o[w][lane].w * f;
     }
   }
   const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(t.x * inv, t.y * inv);
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(tot.x * inv, tot.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(tot.z * inv, tot.w * inv);
   *reinterpret_cast<uint2*>(o) =
       make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
   if (lse && lane == 0) *lse = Lt > 0.f ? (Mt + __log2f(Lt)) * kLn2f : -INFINITY;
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 cudaError_t launch_merge(const MergeParams& p, int32_t /*num_kv_heads*/, cudaStream_t stream) {
   if (p.num_seqs == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_seqs, p.num_q_heads);
+  cfg.gridDim = dim3(p.num_seqs, p.q_len * p.num_q_heads);
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -193,3 +193,10 @@ def make_prologue_inputs(w: Workload, seed: int, eps: float = 1e-6,
     wq = (1 + 0.1 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16)
     wk = (1 + 0.1 * torch.randn(HEAD_DIM, generator=gen)).to(torch.bfloat16)
     return PrologueInputs(q, k, v, wq, wk, eps, rope_base)
+
+
+def make_multi_query(w: Workload, q_len: int, seed: int, q_scale: float = 1.0) -> torch.Tensor:
+    """Seeded N(0,1) queries of q_len new tokens per sequence: bf16 [B][q_len][H_q][D]."""
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.randn(w.num_seqs, q_len, w.num_q_heads, HEAD_DIM, generator=gen)
+            * q_scale).to(torch.bfloat16)
