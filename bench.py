@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--q-lens", default="2,4",
+                    help="query-token counts timed for multi-token decode ('' = none)")
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip timing the fused prologue kernel")
     ap.add_argument("--no-copy-probe", action="store_true",
@@ -509,6 +511,38 @@ def run_hpc(args, ws, rank, local):
             "cores": oracle.num_cpus(), "kind": "oracle",
             "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
                       f"{int(w.seq_lens.sum())} KV tokens), mean of 3 runs, {t:.2f} s each"}
+
+    # ---- multi-token decode (q_len new tokens per sequence share one KV read)
+    if args.q_lens:
+        mt = {}
+        for T in [int(x) for x in args.q_lens.split(",") if x.strip()]:
+            qm = W.make_multi_query(w, T, seed=8000 + T).to(dev)
+            om = torch.empty_like(qm)
+            lm = torch.empty(qm.shape[:3], dtype=torch.float32, device=dev)
+            pm = hpc.hpc_decode_plan_create(B, num_sms, T * hq)
+
+            def mstep():
+                hpc.hpc_decode_step(qm, kc, vc, bt, sl, pm, num_sms, om, lm, stream=stream,
+                                    k_scale=w.k_scale, v_scale=w.v_scale)
+
+            for _ in range(3):
+                flush_l2()
+                mstep()
+            es = [[mk(), mk()] for _ in range(max(5, min(args.steps, 20)))]
+            for a, b_ in es:
+                flush_l2()
+                a.record(stream)
+                mstep()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            assert hpc.hpc_decode_plan_status(pm) == 0
+            pm.destroy()
+            us = statistics.mean(a.elapsed_time(b_) for a, b_ in es) * 1e3
+            mbytes = w.kv_bytes() + T * w.qo_bytes()
+            mt[f"q_len_{T}"] = {"us_per_step": round(us, 2), "algorithmic_bytes": mbytes,
+                                "gbs": round(mbytes / (us * 1e-6) / 1e9, 1),
+                                "us_per_query_token": round(us / T, 2)}
+        line["multi_token"] = mt
 
     # ---- the fused prologue (QK-Norm + RoPE + KV write) for this batch's new tokens
     if not args.no_prologue:
