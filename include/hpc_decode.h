@@ -107,6 +107,19 @@ hpc_status hpc_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t nu
                            hpc_plan_t* plan_out);
 
 /*
+ * hpc_decode_plan_ex -- hpc_decode_plan with a finer unit of work: with
+ * units_per_tile = U > 1 every (64-token tile, KV head) pair is one unit
+ * (U must then equal the cache's number of KV heads), sequence b has n_b * U
+ * units (unit u = head u % U of tile u / U), and the same partition is taken
+ * over the units; segments then hold unit ranges and word 7 of the exported
+ * plan is U. Batches with few tiles per CTA balance U times more finely.
+ * hpc_decode_attn accepts such a plan when num_kv_heads * q_len <= 8
+ * (otherwise HPC_ERR_UNSUPPORTED). U = 1 is hpc_decode_plan.
+ */
+hpc_status hpc_decode_plan_ex(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                              int32_t units_per_tile, hpc_plan_t* plan_out);
+
+/*
  * hpc_decode_plan_create -- an empty dynamic plan able to hold any step with
  * at most `max_seqs` sequences on `num_sms` CTAs; fill it with
  * hpc_decode_plan_device (or hpc_decode_plan_update) every step. All device
@@ -167,8 +180,8 @@ hpc_status hpc_decode_plan_static(const int32_t* seq_lens, int32_t num_seqs, int
 hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, int64_t* len);
 
 /*
- * hpc_decode_plan_compute / hpc_decode_plan_static_compute -- the host
- * planners alone: the same plans as hpc_decode_plan / hpc_decode_plan_static,
+ * hpc_decode_plan_compute / _compute_ex / hpc_decode_plan_static_compute --
+ * the host planners alone: the same plans as hpc_decode_plan / _ex / _static,
  * written in the canonical layout of hpc_decode_plan_export into host memory.
  * No device is touched (usable on machines without a GPU).
  *   buf  host int32 [cap] (may be NULL when cap == 0: only *len is written)
@@ -176,6 +189,9 @@ hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, in
  */
 hpc_status hpc_decode_plan_compute(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                                    int32_t* buf, int64_t cap, int64_t* len);
+hpc_status hpc_decode_plan_compute_ex(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                      int32_t units_per_tile, int32_t* buf, int64_t cap,
+                                      int64_t* len);
 hpc_status hpc_decode_plan_static_compute(const int32_t* seq_lens, int32_t num_seqs,
                                           int32_t num_sms, int32_t num_kv_heads,
                                           int32_t num_splits, int32_t* buf, int64_t cap,
@@ -233,9 +249,11 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
  * of hpc_decode_plan_device, attention and merge, with the planning folded
  * into the attention kernel's start (each CTA derives its own part from the
  * device lengths), so a step is two kernel launches. Afterwards `plan` holds
- * this step's work list, word for word the one hpc_decode_plan_device would
- * write (hpc_decode_plan_export). Batches above 3072 sequences run the
- * separate planner kernel first. Allocates nothing; may be captured in a
+ * this step's work list, word for word the host planner's for the same
+ * lengths (hpc_decode_plan_compute_ex, hpc_decode_plan_export): a plan of
+ * one unit per (tile, KV head) (units_per_tile = num_kv_heads) when
+ * num_kv_heads * q_len <= 8 and num_kv_heads > 1, else of tiles. Batches
+ * above 3072 sequences run the separate planner kernel first. Allocates nothing; may be captured in a
  * CUDA graph after a first call outside the capture.
  *   q, k_cache, v_cache, block_table, out, lse: as hpc_decode_attn
  *   seq_lens  device int32 [B], contiguous

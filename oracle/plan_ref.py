@@ -9,7 +9,9 @@ tiles are given to the CTAs of a persistent grid by actual work; the
 24-ai.news page words it as tiles spread in proportion to each sequence's
 length in the current step). The pages give no cost model or partition
 formula; this oracle takes the plainest reading:
-  * every tile costs one unit (a partial last tile included);
+  * every tile costs one unit (a partial last tile included); optionally a
+    tile is split into one unit per KV head (units_per_tile), a finer grain
+    for batches with few tiles per CTA;
   * tiles are flattened in input sequence order, without sorting;
   * P = min(num_sms, T) parts (no parts when T == 0);
   * part p owns flattened tiles [floor(p*T/P), floor((p+1)*T/P));
@@ -60,10 +62,14 @@ def _seq_offsets(segments: List[Segment], num_seqs: int) -> List[int]:
     return off
 
 
-def dynamic_plan(seq_lens: List[int], num_sms: int) -> Plan:
-    if num_sms <= 0 or any(L < 0 for L in seq_lens):
-        raise ValueError("num_sms must be positive and lengths non-negative")
-    n = tile_counts(seq_lens)
+def dynamic_plan(seq_lens: List[int], num_sms: int, units_per_tile: int = 1) -> Plan:
+    """With units_per_tile = U > 1 every (tile, KV head) pair is one unit of
+    work: sequence b has n_b * U units, unit u being head u % U of tile u // U,
+    and the same partition is applied to the units (segments then hold unit
+    ranges)."""
+    if num_sms <= 0 or units_per_tile <= 0 or any(L < 0 for L in seq_lens):
+        raise ValueError("num_sms and units_per_tile must be positive, lengths non-negative")
+    n = [c * units_per_tile for c in tile_counts(seq_lens)]
     T = sum(n)
     P = min(num_sms, T)
     seq_start = [0]

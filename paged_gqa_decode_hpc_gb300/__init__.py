@@ -20,7 +20,7 @@ from . import _build
 
 __all__ = [
     "build", "load_library", "HpcError", "Plan",
-    "hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_plan_create",
+    "hpc_decode_plan", "hpc_decode_plan_ex", "hpc_decode_plan_compute_ex", "hpc_decode_plan_static", "hpc_decode_plan_create",
     "hpc_decode_plan_device", "hpc_decode_plan_update", "hpc_decode_plan_export",
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
@@ -87,6 +87,8 @@ def load_library():
         T = ctypes.POINTER(HpcTensor)
         sigs = {
             "hpc_decode_plan": [pi32, i32, i32, ctypes.POINTER(P)],
+            "hpc_decode_plan_ex": [pi32, i32, i32, i32, ctypes.POINTER(P)],
+            "hpc_decode_plan_compute_ex": [pi32, i32, i32, i32, pi32, i64, pi64],
             "hpc_decode_plan_create": [i32, i32, i32, ctypes.POINTER(P)],
             "hpc_decode_plan_device": [P, i32, i32, P, P],
             "hpc_decode_plan_update": [pi32, i32, i32, P, P],
@@ -176,6 +178,15 @@ def hpc_decode_plan(seq_lens: Sequence[int], num_sms: int) -> Plan:
     return Plan(h, HPC_PLAN_DYNAMIC)
 
 
+def hpc_decode_plan_ex(seq_lens: Sequence[int], num_sms: int, units_per_tile: int) -> Plan:
+    """Balanced plan over (tile, KV head) units when units_per_tile = H_kv."""
+    a = _i32_array(seq_lens)
+    h = ctypes.c_void_p()
+    _check(load_library().hpc_decode_plan_ex(_p_i32(a), a.size, int(num_sms),
+                                             int(units_per_tile), ctypes.byref(h)))
+    return Plan(h, HPC_PLAN_DYNAMIC)
+
+
 def hpc_decode_plan_static(seq_lens: Sequence[int], num_sms: int, num_kv_heads: int,
                            num_splits: int = 0) -> Plan:
     a = _i32_array(seq_lens)
@@ -225,6 +236,13 @@ def hpc_decode_plan_export(plan: Plan) -> np.ndarray:
 def hpc_decode_plan_compute(seq_lens: Sequence[int], num_sms: int) -> np.ndarray:
     a = _i32_array(seq_lens)
     return _canonical(load_library().hpc_decode_plan_compute, _p_i32(a), a.size, int(num_sms))
+
+
+def hpc_decode_plan_compute_ex(seq_lens: Sequence[int], num_sms: int,
+                               units_per_tile: int) -> np.ndarray:
+    a = _i32_array(seq_lens)
+    return _canonical(load_library().hpc_decode_plan_compute_ex, _p_i32(a), a.size, int(num_sms),
+                      int(units_per_tile))
 
 
 def hpc_decode_plan_static_compute(seq_lens: Sequence[int], num_sms: int, num_kv_heads: int,

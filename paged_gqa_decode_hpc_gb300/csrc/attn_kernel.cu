@@ -612,7 +612,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       if (b < B) {
         const int32_t len = p.seq_lens[b];
         if (len < 0) s_bad = 1;
-        n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) : 0;
+        n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) * p.plan_units : 0;
       }
       int32_t tot;
       const int32_t incl = cta_inclusive_scan(n, warp_tot, &tot);
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       if (bad) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
       w[kMagic] = kPlanMagic; w[kKind] = HPC_PLAN_DYNAMIC; w[kNumSeqs] = B;
       w[kNumParts] = (int32_t)P; w[kNumTiles] = (int32_t)T; w[kNumSegs] = (int32_t)gcarry;
-      w[kNumSms] = p.plan_num_sms; w[kSplits] = 0;
+      w[kNumSms] = p.plan_num_sms; w[kSplits] = p.plan_units > 1 ? p.plan_units : 0;
       w[p.cu_off] = 0; w[p.seq_off] = 0; w[p.part_off + P] = (int32_t)gcarry;
     }
     if (part >= P) return;  // uniform over the CTA
@@ -691,8 +691,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     SegCursor sc = cur0;
     int b, tb, te, slot;
     bool whole;
+    const int U = p.plan_units;  // 1: segments hold tiles; U > 1: (tile, head) units
     while (sc.next(b, tb, te, whole, slot)) {
-      const int n = te - tb;
+      // tiles [t0, t0 + n) touched by the segment; with U > 1 only the heads of
+      // units in [tb, te) are loaded at the first and last tile
+      const int t0 = tb / U;
+      const int n = (te - 1) / U + 1 - t0;
       if (sc.fused && lane == 0) {  // this part's segment records of the plan
         int4 rec;
         rec.x = b;
@@ -707,7 +711,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           const int i = i0 + lane;
           int blk = p.num_blocks;  // out of range: TMA fills zeros
           if (i < n) {
-            const int t = tb + i;
+            const int t = t0 + i;
             if (t < p.max_blocks) {
               const int v = __ldg(btrow + t);
               if (v >= 0 && v < p.num_blocks) blk = v;
@@ -719,7 +723,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           const int cnt = n - i0 < 32 ? n - i0 : 32;
           for (int ii = 0; ii < cnt; ++ii) {
             const int bk = __shfl_sync(0xffffffffu, blk, ii);
-            for (int hl = 0; hl < hpass; ++hl, ++g) {
+            const int ta = t0 + i0 + ii;  // absolute tile
+            const int hlo = U > 1 && ta * U < tb ? tb - ta * U : 0;
+            const int hhi = U > 1 && (ta + 1) * U > te ? te - ta * U : hpass;
+            for (int hl = hlo; hl < hhi; ++hl, ++g) {
               if (lane != 0 || stop) continue;
               const int h = h_begin + pass * hpass + hl;
               const uint32_t slot = g % STAGES;
@@ -770,12 +777,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   SegCursor sc = cur0;
   int b, tb, te, seg;
   bool whole;
+  const int U = p.plan_units;
   while (sc.next(b, tb, te, whole, seg)) {
-    const int n = te - tb;
+    const int t0 = tb / U;
+    const int n = (te - 1) / U + 1 - t0;  // tiles touched by the segment
     const int len = p.seq_lens[b];
+    // this warp's tiles [i_lo, i_hi) (relative to t0): all of them in tile
+    // plans; with U > 1 the tiles t whose unit t * U + h lies in [tb, te)
+    int i_lo = 0, i_hi = n;
+    if (U > 1) {
+      i_lo = (tb + (U - 1 - hl)) / U - t0;
+      i_hi = (te - 1 - hl >= 0 ? (te - 1 - hl) / U + 1 : 0) - t0;
+    }
     if (!sc.fused && warp == 0 && lane == 0) {
       const int n_plan = p.plan[p.cu_off + b + 1] - p.plan[p.cu_off + b];
-      const int n_dev = len > 0 ? (len + kBlockTokens - 1) / kBlockTokens : 0;
+      const int n_dev = (len > 0 ? (len + kBlockTokens - 1) / kBlockTokens : 0) * U;
       if (n_plan != n_dev) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
     }
     for (int pass = 0; pass < npass; ++pass) {
@@ -787,12 +803,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       // causal limit of this warp's query token: the q_len new tokens are the
       // last q_len positions of the sequence
       const int len_t = len - (p.q_len - 1 - tok);
-      if (active && tphase < n) {
+      if (active && i_lo + tphase < i_hi) {
         uint32_t qf[8][2];
         const float qinv = load_q<FP8>(p, b, tok, h, lane, qf);
         const float sl2 = p.score_scale_log2 * qinv;
-        for (int i = tphase; i < n; i += tph) {
-          const uint32_t gu = gbase + (uint32_t)(i * hpass + hl);
+        for (int i = i_lo + tphase; i < i_hi; i += tph) {
+          // position of unit (tile t0 + i, head hl) in the order of issue
+          const uint32_t gu = U > 1 ? gbase + (uint32_t)((t0 + i) * U + hl - tb)
+                                    : gbase + (uint32_t)(i * hpass + hl);
           const uint32_t slot = gu % STAGES;
           if (dead) continue;
           const bool ok =
@@ -803,7 +821,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             dead = true;
             continue;
           }
-          const int valid = len_t - (tb + i) * kBlockTokens;
+          const int valid = len_t - (t0 + i) * kBlockTokens;
           if (valid > 0) {
             const uint32_t kb = smem_base + slot * kStage;
             compute_unit<FP8>(kb, kb + kTile, qf, valid, sl2, m, l, acc, lane);
@@ -812,7 +830,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
       }
-      gbase += (uint32_t)(n * hpass);
+      gbase += U > 1 ? (uint32_t)(te - tb) : (uint32_t)(n * hpass);
       // reduce the row sums over the 8 lanes sharing a column pair
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {

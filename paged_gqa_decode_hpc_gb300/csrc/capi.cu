@@ -219,16 +219,22 @@ hpc_status hpc_device_sm_count(int32_t* num_sms) {
 
 hpc_status hpc_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                            hpc_plan_t* plan_out) {
+  return hpc_decode_plan_ex(seq_lens, num_seqs, num_sms, 1, plan_out);
+}
+
+hpc_status hpc_decode_plan_ex(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                              int32_t units_per_tile, hpc_plan_t* plan_out) {
   if (!plan_out) return fail(HPC_ERR_INVALID_ARG, "plan_out is null");
   *plan_out = nullptr;
   if (num_seqs < 0 || (num_seqs > 0 && !seq_lens))
     return fail(HPC_ERR_INVALID_ARG, "seq_lens is null or num_seqs < 0");
   if (num_sms <= 0) return fail(HPC_ERR_INVALID_ARG, "num_sms must be positive");
+  if (units_per_tile <= 0) return fail(HPC_ERR_INVALID_ARG, "units_per_tile must be positive");
   int64_t T = 0;
   for (int32_t b = 0; b < num_seqs; ++b) {
     if (seq_lens[b] < 0)
       return fail(HPC_ERR_INVALID_ARG, "negative sequence length at index " + std::to_string(b));
-    T += (seq_lens[b] + (int64_t)kBlockTokens - 1) / kBlockTokens;
+    T += (seq_lens[b] + (int64_t)kBlockTokens - 1) / kBlockTokens * units_per_tile;
   }
   PlanLayout L;
   L.cap_seqs = num_seqs;
@@ -236,10 +242,13 @@ hpc_status hpc_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t nu
   L.cap_segs = (int32_t)dynamic_max_segs(num_seqs, L.cap_parts);
   std::vector<int32_t> w((size_t)L.words(), 0);
   std::string err;
-  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err);
+  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err,
+                                    units_per_tile);
   if (st != HPC_OK) return fail(st, err);
-  return new_host_plan(w.data(), L, HPC_PLAN_DYNAMIC, num_sms, num_seqs, w[kNumParts],
-                       w[kNumSegs], 0, plan_out);
+  st = new_host_plan(w.data(), L, HPC_PLAN_DYNAMIC, num_sms, num_seqs, w[kNumParts],
+                     w[kNumSegs], 0, plan_out);
+  if (st == HPC_OK) (*plan_out)->units = units_per_tile;
+  return st;
 }
 
 hpc_status hpc_decode_plan_static(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
@@ -317,6 +326,7 @@ hpc_status hpc_decode_plan_device(const int32_t* seq_lens_dev, int32_t num_seqs,
   plan->num_sms = num_sms;
   plan->host_num_parts = -1;
   plan->host_num_segs = -1;
+  plan->units = 1;
   return HPC_OK;
 }
 
@@ -340,6 +350,7 @@ hpc_status hpc_decode_plan_update(const int32_t* seq_lens, int32_t num_seqs, int
   plan->num_sms = num_sms;
   plan->host_num_parts = plan->h_pinned[kNumParts];
   plan->host_num_segs = plan->h_pinned[kNumSegs];
+  plan->units = 1;
   return HPC_OK;
 }
 
@@ -355,6 +366,12 @@ hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, in
 
 hpc_status hpc_decode_plan_compute(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                                    int32_t* buf, int64_t cap, int64_t* len) {
+  return hpc_decode_plan_compute_ex(seq_lens, num_seqs, num_sms, 1, buf, cap, len);
+}
+
+hpc_status hpc_decode_plan_compute_ex(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
+                                      int32_t units_per_tile, int32_t* buf, int64_t cap,
+                                      int64_t* len) {
   if (!len) return fail(HPC_ERR_INVALID_ARG, "len is null");
   if (num_seqs < 0 || (num_seqs > 0 && !seq_lens))
     return fail(HPC_ERR_INVALID_ARG, "seq_lens is null or num_seqs < 0");
@@ -365,7 +382,8 @@ hpc_status hpc_decode_plan_compute(const int32_t* seq_lens, int32_t num_seqs, in
   L.cap_segs = (int32_t)dynamic_max_segs(num_seqs, num_sms);
   std::vector<int32_t> w((size_t)L.words(), 0);
   std::string err;
-  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err);
+  hpc_status st = plan_dynamic_host(seq_lens, num_seqs, num_sms, w.data(), L, &err,
+                                    units_per_tile);
   if (st != HPC_OK) return fail(st, err);
   return write_canonical(w.data(), L, buf, cap, len);
 }
@@ -495,6 +513,13 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
                                          " sequences, q has " + std::to_string(B));
   if (plan->kind == HPC_PLAN_STATIC && plan->static_kv_heads != Hkv)
     return fail(HPC_ERR_INVALID_ARG, "static plan was built for another number of kv heads");
+  if (plan->units > 1) {
+    const WarpLayout wl = warp_layout((int)Hkv, (int)T, 8);
+    if (plan->units != Hkv || wl.npass != 1 || wl.tph != 1)
+      return fail(HPC_ERR_UNSUPPORTED, "a plan with " + std::to_string(plan->units) +
+                                           " units per tile needs num_kv_heads == units and "
+                                           "num_kv_heads * q_len <= 8");
+  }
   if (fp8 && (!std::isfinite(k_cache->scale) || !std::isfinite(v_cache->scale)))
     return fail(HPC_ERR_INVALID_ARG, "FP8 scales must be finite");
   if (B == 0) return HPC_OK;
@@ -553,6 +578,7 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     p.kv_swap = swap;
     p.fused_plan = fused_num_sms > 0;
     p.plan_num_sms = fused_num_sms;
+    p.plan_units = plan->kind == HPC_PLAN_STATIC ? 1 : plan->units;
     p.plan_out = plan->d_words;
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
     p.score_scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_cache->scale : 1.0f);
@@ -626,13 +652,31 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
     return fail(HPC_ERR_INVALID_ARG, "num_seqs exceeds the plan's max_seqs");
   if (num_sms <= 0 || num_sms > plan->layout.cap_parts)
     return fail(HPC_ERR_INVALID_ARG, "num_sms must be in [1, plan num_sms]");
+  // One unit per (tile, KV head) when the kernel's warp layout takes all KV
+  // heads in one pass with one warp per (head, token): an 8x finer partition.
+  int32_t units = 1;
+  if (k_cache && k_cache->ndim == 4) {
+    const int64_t hkv = k_cache->shape[1], T = q->ndim == 4 ? q->shape[1] : 1;
+    if (hkv > 1 && hkv <= 64 && T >= 1 && T <= kMaxQueryTokens) {
+      const WarpLayout wl = warp_layout((int)hkv, (int)T, 8);
+      if (wl.npass == 1 && wl.tph == 1) units = (int32_t)hkv;
+    }
+  }
   if (B > kFusedPlanMaxSeqs || B == 0) {  // separate planner kernel
-    hpc_status st = hpc_decode_plan_device((const int32_t*)seq_lens->data, (int32_t)B, num_sms,
-                                           plan, stream);
-    if (st != HPC_OK) return st;
+    cudaError_t e = launch_plan_device((const int32_t*)seq_lens->data, (int32_t)B, num_sms,
+                                       plan->d_words, plan->layout, plan->d_err,
+                                       (cudaStream_t)stream, units);
+    if (e != cudaSuccess)
+      return fail(HPC_ERR_CUDA, std::string("device planner launch: ") + cudaGetErrorString(e));
+    plan->num_seqs = (int32_t)B;
+    plan->num_sms = num_sms;
+    plan->host_num_parts = -1;
+    plan->host_num_segs = -1;
+    plan->units = units;
     return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
                      0);
   }
+  plan->units = units;
   plan->num_seqs = (int32_t)B;
   plan->num_sms = num_sms;
   plan->host_num_parts = -1;

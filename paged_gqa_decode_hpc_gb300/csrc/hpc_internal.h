@@ -51,6 +51,7 @@ struct hpc_plan_s {
   int32_t host_num_parts = -1;   // -1: only the device knows (device planner)
   int32_t host_num_segs = -1;
   int32_t static_kv_heads = 0;   // static plans: grid.y
+  int32_t units = 1;             // units per tile of the current work list
   int32_t* d_words = nullptr;    // plan buffer
   int32_t* h_pinned = nullptr;   // staging for hpc_decode_plan_update
   cudaEvent_t copy_done = nullptr;  // last upload from h_pinned
@@ -82,6 +83,7 @@ struct AttnParams {
   int32_t fused_plan;           // 1: each CTA plans its own part from seq_lens and
                                 //    the CTAs write the plan words (plan_out)
   int32_t plan_num_sms;         // fused: parts cap (P = min(plan_num_sms, T))
+  int32_t plan_units;           // units per tile of the plan (1: tiles; H_kv: (tile, head))
   int32_t* plan_out;            // fused: plan buffer written by the kernel
   int32_t kv_swap;              // tensor map dims are (d, head, slot, block)
   float score_scale_log2;       // softmax_scale * log2(e) (* k_scale for FP8)
@@ -144,8 +146,11 @@ cudaError_t launch_prologue(const PrologueParams& p, cudaStream_t stream);
 
 // Host planners (plan_host.cu). Fill `words` (canonical layout sized by the
 // returned length) or report an error message.
+// units_per_tile = U > 1: every (tile, KV head) pair is one unit of the
+// partition (head-granular plan); header word kSplits then holds U.
 hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
-                             int32_t* words, const PlanLayout& L, std::string* err);
+                             int32_t* words, const PlanLayout& L, std::string* err,
+                             int32_t units_per_tile = 1);
 hpc_status plan_static_host(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                             int32_t num_kv_heads, int32_t num_splits,
                             int32_t** words_out, PlanLayout* L_out, std::string* err);
@@ -154,7 +159,7 @@ int64_t dynamic_max_segs(int32_t num_seqs, int32_t num_parts);
 // Launchers (kernels .cu files).
 cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                                int32_t* words, const PlanLayout& L, int32_t* err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int32_t units_per_tile = 1);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                              bool fp8, int grid_x, int grid_y, cudaStream_t stream);
 // Query tokens per sequence the attention kernel supports (one consumer warp

@@ -61,7 +61,7 @@ __device__ __forceinline__ int32_t block_inclusive_scan(int32_t v, int32_t* warp
 
 __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
     const int32_t* __restrict__ seq_lens, int32_t B, int32_t num_sms, int32_t* __restrict__ w,
-    PlanLayout L, int32_t* __restrict__ err) {
+    PlanLayout L, int32_t* __restrict__ err, int32_t units) {
   extern __shared__ int32_t dsm[];
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t bad;
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
     if (b < B) {
       const int32_t len = seq_lens[b];
       if (len < 0) bad = 1;  // benign race: every writer stores 1
-      n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) : 0;
+      n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) * units : 0;
     }
     int32_t chunk_total;
     const int32_t incl = block_inclusive_scan(n, warp_tot, &chunk_total);
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
       atomicOr(err, HPC_DEVCHK_BAD_LENGTH);
       w[kMagic] = kPlanMagic; w[kKind] = HPC_PLAN_DYNAMIC; w[kNumSeqs] = B;
       w[kNumParts] = 0; w[kNumTiles] = 0; w[kNumSegs] = 0; w[kNumSms] = num_sms;
-      w[kSplits] = 0; part_off[0] = 0;
+      w[kSplits] = units > 1 ? units : 0; part_off[0] = 0;
     }
     for (int32_t b = tid; b <= B; b += kPlanThreads) so_g[b] = 0;
     return;
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
     w[kNumTiles] = (int32_t)T;
     w[kNumSegs] = (int32_t)gcarry;
     w[kNumSms] = num_sms;
-    w[kSplits] = 0;
+    w[kSplits] = units > 1 ? units : 0;
   }
 }
 
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_device_kernel(
 
 cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_t num_sms,
                                int32_t* words, const PlanLayout& L, int32_t* err,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int32_t units_per_tile) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(kPlanThreads);
@@ -201,7 +201,8 @@ cudaError_t launch_plan_device(const int32_t* seq_lens, int32_t num_seqs, int32_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, plan_device_kernel, seq_lens, num_seqs, num_sms, words, L, err);
+  return cudaLaunchKernelEx(&cfg, plan_device_kernel, seq_lens, num_seqs, num_sms, words, L, err,
+                            units_per_tile);
 }
 
 }  // namespace hpc

@@ -24,7 +24,11 @@ int64_t dynamic_max_segs(int32_t num_seqs, int32_t num_parts) {
 }
 
 hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t B, int32_t num_sms, int32_t* w,
-                             const PlanLayout& L, std::string* err) {
+                             const PlanLayout& L, std::string* err, int32_t units_per_tile) {
+  if (units_per_tile <= 0) {
+    *err = "units_per_tile must be positive";
+    return HPC_ERR_INVALID_ARG;
+  }
   if (B < 0 || (B > 0 && !seq_lens)) {
     *err = "seq_lens is null or num_seqs < 0";
     return HPC_ERR_INVALID_ARG;
@@ -45,7 +49,7 @@ hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t B, int32_t num_sms
       *err = "negative sequence length at index " + std::to_string(b);
       return HPC_ERR_INVALID_ARG;
     }
-    total += (seq_lens[b] + (int64_t)kBlockTokens - 1) / kBlockTokens;
+    total += (seq_lens[b] + (int64_t)kBlockTokens - 1) / kBlockTokens * units_per_tile;
     if (total > INT32_MAX) {
       *err = "total tile count exceeds 2^31-1";
       return HPC_ERR_INVALID_ARG;
@@ -101,7 +105,7 @@ hpc_status plan_dynamic_host(const int32_t* seq_lens, int32_t B, int32_t num_sms
   w[kNumTiles] = (int32_t)T;
   w[kNumSegs] = (int32_t)g;
   w[kNumSms] = num_sms;
-  w[kSplits] = 0;
+  w[kSplits] = units_per_tile > 1 ? units_per_tile : 0;
   return HPC_OK;
 }
 

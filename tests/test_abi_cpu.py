@@ -40,6 +40,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def oracle_words(plan, lengths, num_sms, kind, splits=0):
+    """Canonical words of an oracle plan (word 7: static split count, or the
+    units per tile of a unit plan)."""
     w = [0x48504344, kind, len(lengths), plan.num_parts, plan.num_tiles, len(plan.segments),
          num_sms, splits]
     w += plan.part_seg_off + plan.seq_seg_off
@@ -118,3 +120,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         hpc.load_library()
+
+
+def test_host_unit_plans_match_oracle(lib):
+    for lens, sms in _cases()[:60]:
+        for u in (2, 4, 8):
+            got = hpc.hpc_decode_plan_compute_ex(lens, sms, u)
+            ref = oracle_words(plan_ref.dynamic_plan(lens, sms, units_per_tile=u), lens, sms, 0, u)
+            assert np.array_equal(got, ref), (lens[:8], sms, u)
+        assert np.array_equal(hpc.hpc_decode_plan_compute_ex(lens, sms, 1),
+                              hpc.hpc_decode_plan_compute(lens, sms))

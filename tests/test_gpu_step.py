@@ -24,6 +24,30 @@ def _cfg(hq=64, hkv=8, fp8=False):
     return W.Config(92, "step", hq, hkv, "fp8_e4m3" if fp8 else "bf16")
 
 
+def step_units(hkv, q_len=1, nc=8):
+    """Units per tile the step chooses: H_kv when one pass of one warp per
+    (head, token) covers all KV heads, else 1 (mirrors the library's rule)."""
+    hpass = max(1, nc // q_len)
+    hpass = min(hpass, hkv)
+    while hkv % hpass:
+        hpass -= 1
+    npass, tph = hkv // hpass, (nc // hpass) // q_len
+    return hkv if hkv > 1 and npass == 1 and tph == 1 else 1
+
+
+def run_plan_ex(w, units, num_sms):
+    d = device_workload(w)
+    B, hq = w.q.shape[0], w.q.shape[1]
+    out = torch.full((B, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, hq), float("nan"), dtype=torch.float32, device="cuda")
+    with hpc.hpc_decode_plan_ex(w.seq_lens.tolist(), num_sms, units) as p:
+        hpc.hpc_decode_attn(d["q"], d["k"], d["v"], d["bt"], d["sl"], p, out, lse,
+                            k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        assert hpc.hpc_decode_plan_status(p) == 0
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
 def run_step(w, d=None, num_sms=None, plan=None):
     d = d or device_workload(w)
     sms_all = hpc.hpc_device_sm_count()
@@ -59,9 +83,10 @@ def test_step_parity_and_plan_words(lens, hq, hkv, fp8, sms):
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label=f"step {lens[:4]}")
     n = sms or hpc.hpc_device_sm_count()
-    assert np.array_equal(words, hpc.hpc_decode_plan_compute(lens, n))
-    # the planner-kernel path gives the same bits
-    out2, lse2 = run_cuda(w, plan="device", num_sms=n)
+    u = step_units(hkv)
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(lens, n, u))
+    # a host plan with the same units gives the same bits
+    out2, lse2 = run_plan_ex(w, u, n)
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
@@ -71,8 +96,8 @@ def test_step_skewed_config():
     out, lse, words, err = run_step(w)
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label="step skewed")
-    assert np.array_equal(words, hpc.hpc_decode_plan_compute(w.seq_lens.tolist(),
-                                                              hpc.hpc_device_sm_count()))
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(w.seq_lens.tolist(),
+                                                                 hpc.hpc_device_sm_count(), 8))
 
 
 def test_step_many_sequences_uses_the_planner_kernel():
@@ -121,3 +146,30 @@ def test_step_reuses_one_plan_across_batches_and_graph_capture():
     ref_out, ref_lse = oracle.decode_workload(w)
     assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse)
     plan.destroy()
+
+
+@pytest.mark.parametrize("lens,fp8,sms", [
+    ([512] * 64, False, None), ([512] * 64, True, 7), ([1, 63, 64, 65, 700, 3001, 0], False, 3),
+    ([131072] + [4096] * 31, False, None)])
+def test_unit_plans_parity(lens, fp8, sms):
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=lens, seed=48)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse = run_plan_ex(w, 8, sms or hpc.hpc_device_sm_count())
+    assert_parity(out, lse, ref_out, ref_lse, label=f"unit plan {lens[:3]}")
+
+
+def test_unit_plan_rejected_for_other_layouts():
+    w = W.make_workload(_cfg(16, 2), lengths=[100, 300], seed=49)
+    with pytest.raises(hpc.HpcError) as ei:
+        run_plan_ex(w, 2, 16)  # 2 KV heads: warps split tiles, unit plans unsupported
+    assert ei.value.status == hpc.HPC_ERR_UNSUPPORTED
+
+
+def test_step_many_sequences_unit_plan_through_the_planner_kernel():
+    lens = [(i * 53) % 200 + 1 for i in range(3300)]
+    w = W.make_workload(_cfg(64, 8), lengths=lens, seed=50)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label="step 3300 seqs, unit plan")
+    assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(lens, hpc.hpc_device_sm_count(), 8))

@@ -22,8 +22,8 @@ def _lengths(case):
     return out
 
 
-def check_dynamic(lengths, num_sms, plan):
-    n = plan_ref.tile_counts(lengths)
+def check_dynamic(lengths, num_sms, plan, units_per_tile=1):
+    n = [c * units_per_tile for c in plan_ref.tile_counts(lengths)]
     T = sum(n)
     assert plan.num_tiles == T
     assert plan.num_parts == min(num_sms, T)
@@ -136,3 +136,21 @@ def test_static_plan_rule_and_coverage():
             if sizes:
                 assert max(sizes) - min(sizes) <= 1
             assert all(s.whole == (len(segs) == 1) for s in segs)
+
+
+def test_units_per_tile_plans():
+    # uniform 64 x 512 with one unit per (tile, kv head): 4096 units over 152
+    # parts of 26 or 27 units (4096 = 152 * 26 + 144)
+    L = [512] * 64
+    plan = plan_ref.dynamic_plan(L, 152, units_per_tile=8)
+    sizes = check_dynamic(L, 152, plan, units_per_tile=8)
+    assert plan.num_tiles == 4096 and min(sizes) == 26 and max(sizes) == 27
+    assert sizes.count(27) == 144
+    import random
+    rng = random.Random(9)
+    for _ in range(100):
+        lens = [rng.choice([0, rng.randint(1, 64), rng.randint(1, 3000)]) for _ in range(rng.randint(1, 30))]
+        sms, u = rng.randint(1, 160), rng.choice([1, 2, 4, 8])
+        check_dynamic(lens, sms, plan_ref.dynamic_plan(lens, sms, units_per_tile=u), units_per_tile=u)
+    # U = 1 is the tile plan
+    assert plan_ref.dynamic_plan([700, 3], 5, 1) == plan_ref.dynamic_plan([700, 3], 5)
