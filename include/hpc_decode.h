@@ -291,9 +291,9 @@ hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, vo
  * caching allocator, where a direct cudaMalloc/cudaFree would synchronise the
  * device or fail under memory pressure.
  *
- * Its work list, partial results, merge counters and error word live in one
- * file-scope device array of about 13.9 MB that every GPU loading this library
- * holds until the process exits (the counters are cleared at every call). Limits (HPC_ERR_INVALID_ARG beyond them, with a
+ * Its work list, partial results and error word live in one file-scope
+ * device array of about 13.9 MB that every GPU loading this library holds
+ * until the process exits. Limits (HPC_ERR_INVALID_ARG beyond them, with a
  * message): num_seqs <= HPC_NOALLOC_MAX_SEQS, CTAs <= HPC_NOALLOC_MAX_CTAS,
  * num_q_heads <= HPC_NOALLOC_MAX_Q_HEADS.
  *

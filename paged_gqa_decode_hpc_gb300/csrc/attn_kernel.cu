@@ -539,71 +539,6 @@ __device__ __forceinline__ void write_result(const AttnParams& p, bool whole, in
   }
 }
 
-// In-CTA log-sum-exp merge of one split sequence (2..kFuseMergeMax segments,
-// partial rows at slots s0..s0+ns-1), run by the CTA that wrote its last
-// partial. Warp w takes the (token, KV head) groups w, w + NC, ...; a lane
-// owns 4 output columns of each of the group's 8 query heads. Partials written
-// by other SMs are read through L2 (ld.global.cg).
-template <int NC>
-__device__ __forceinline__ void merge_sequence_in_cta(const AttnParams& p, int b, int s0, int ns,
-                                                      int warp, int lane) {
-  const int groups = p.q_len * p.num_kv_heads;
-  const int64_t hv = (int64_t)p.q_len * p.num_q_heads;
-  for (int gidx = warp; gidx < groups; gidx += NC) {
-    const int t = gidx / p.num_kv_heads, h = gidx % p.num_kv_heads;
-#pragma unroll 1
-    for (int quarter = 0; quarter < 4; ++quarter) {  // 2 query heads at a time
-      float mm[2][kFuseMergeMax], ll[2][kFuseMergeMax];
-      float4 oo[2][kFuseMergeMax];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int64_t jv = (int64_t)t * p.num_q_heads + h * kGroup + quarter * 2 + k;
-#pragma unroll
-        for (int i = 0; i < kFuseMergeMax; ++i) {
-          if (i < ns) {
-            const int64_t r = (int64_t)(s0 + i) * hv + jv;
-            mm[k][i] = __ldcg(p.ws_m + r);
-            ll[k][i] = __ldcg(p.ws_l + r);
-            oo[k][i] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + r * kHeadDim) + lane);
-          } else {
-            mm[k][i] = -INFINITY;
-            ll[k][i] = 0.f;
-            oo[k][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int j = h * kGroup + quarter * 2 + k;
-        float M = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kFuseMergeMax; ++i) M = fmaxf(M, mm[k][i]);
-        float L = 0.f;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int i = 0; i < kFuseMergeMax; ++i) {
-            const float w = mm[k][i] == -INFINITY ? 0.f : ex2(mm[k][i] - M);
-            L += ll[k][i] * w;
-            a.x += oo[k][i].x * w; a.y += oo[k][i].y * w;
-            a.z += oo[k][i].z * w; a.w += oo[k][i].w * w;
-          }
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-        __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)t * p.o_st +
-                           (int64_t)j * p.o_sh + 4 * lane;
-        *reinterpret_cast<uint2*>(o) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
-                                                  *reinterpret_cast<const uint32_t*>(&hi));
-        if (p.lse && lane == 0)
-          p.lse[(int64_t)b * p.l_sb + (int64_t)t * p.l_st + (int64_t)j * p.l_sh] =
-              L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
-      }
-    }
-  }
-}
-
 template <bool FP8, int STAGES, int NC, bool COMBINE>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     attn_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
@@ -619,7 +554,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   const uint32_t bar_empty = bar_full + STAGES * 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kAbortOff);
   const uint32_t issued_word = smem_base + Cfg::kIssuedOff;
-  __shared__ int s_merge_here;  // this CTA completed a split sequence: merge it
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -958,31 +892,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           if (!*abort_flag) write_result<FP8>(p, whole, b, tok, h, seg, m, l, acc, lane);
         }
         named_bar_sync(1, NC * 32);
-      }
-    }
-    // A short split sequence is merged by the CTA that writes its last partial:
-    // every writer fences, one thread counts the segment, the CTA that brings
-    // the count to ns resets it and merges (no CTA waits for another).
-    if (!whole && p.seq_cnt) {
-      const int s0 = sc.fused ? sc.so[b] : p.plan[p.seq_off + b];
-      const int ns = sc.fused ? sc.so[b + 1] - s0 : p.plan[p.seq_off + b + 1] - s0;
-      if (ns <= p.fuse_merge_max) {
-        __threadfence();  // this thread's partial rows before the count
-        named_bar_sync(2, NC * 32);
-        if (warp == 0 && lane == 0) {
-          int last = 0;
-          if (!*abort_flag) {
-            const int old = atomicAdd(p.seq_cnt + b, 1);
-            last = old == ns - 1;
-            if (last) {
-              atomicExch(p.seq_cnt + b, 0);  // ready for the next step
-              __threadfence();
-            }
-          }
-          s_merge_here = last;
-        }
-        named_bar_sync(2, NC * 32);
-        if (s_merge_here) merge_sequence_in_cta<NC>(p, b, s0, ns, warp, lane);
       }
     }
   }

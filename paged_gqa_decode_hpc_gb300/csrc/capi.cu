@@ -57,7 +57,6 @@ void free_plan(hpc_plan_s* pl) {
   if (!pl) return;
   if (pl->d_words) cudaFree(pl->d_words);
   if (pl->d_err) cudaFree(pl->d_err);
-  if (pl->d_cnt) cudaFree(pl->d_cnt);
   if (pl->d_ws) cudaFree(pl->d_ws);
   if (pl->h_pinned) cudaFreeHost(pl->h_pinned);
   if (pl->copy_done) cudaEventDestroy(pl->copy_done);
@@ -70,9 +69,6 @@ hpc_status alloc_plan_buffers(hpc_plan_s* pl) {
   HPC_CUDA_TRY(cudaMalloc(&pl->d_words, (size_t)pl->layout.words() * sizeof(int32_t)));
   HPC_CUDA_TRY(cudaMalloc(&pl->d_err, sizeof(int32_t)));
   HPC_CUDA_TRY(cudaMemset(pl->d_err, 0, sizeof(int32_t)));
-  const size_t nc = (size_t)std::max<int32_t>(pl->layout.cap_seqs, 1);
-  HPC_CUDA_TRY(cudaMalloc(&pl->d_cnt, nc * sizeof(int32_t)));
-  HPC_CUDA_TRY(cudaMemset(pl->d_cnt, 0, nc * sizeof(int32_t)));
   return HPC_OK;
 }
 
@@ -414,9 +410,6 @@ hpc_status hpc_decode_plan_status(hpc_plan_t plan, int32_t* device_error) {
   int32_t v = 0;
   HPC_CUDA_TRY(cudaMemcpy(&v, plan->d_err, sizeof v, cudaMemcpyDeviceToHost));
   HPC_CUDA_TRY(cudaMemset(plan->d_err, 0, sizeof v));
-  if (v != 0 && plan->d_cnt)  // an aborted step may leave merge counters set
-    HPC_CUDA_TRY(cudaMemset(plan->d_cnt, 0,
-                            (size_t)std::max<int32_t>(plan->layout.cap_seqs, 1) * sizeof(int32_t)));
   *device_error = v;
   if (v != 0)
     return fail(HPC_ERR_DEVICE_CHECK, "device check fired (bits " + std::to_string(v) + ")");
@@ -596,9 +589,6 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     p.ws_l = p.ws_m + cs * T * Hq;
     p.err = plan->d_err;
     p.timeout_ns = wait_limit_ns();
-    const bool fuse = plan->kind != HPC_PLAN_STATIC && plan->d_cnt;
-    p.seq_cnt = fuse ? plan->d_cnt : nullptr;
-    p.fuse_merge_max = fuse ? kFuseMergeMax : 0;
     if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
     cudaError_t ce = launch_attention(p, tk, tv, fp8, gx, gy, s);
     if (ce != cudaSuccess)
@@ -616,7 +606,6 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
   mp.l_st = l_st;
   mp.l_sh = l_sh;
   mp.q_len = (int32_t)T;
-  mp.fused_max = (plan->kind != HPC_PLAN_STATIC && plan->d_cnt) ? kFuseMergeMax : 0;
   mp.plan = plan->d_words;
   mp.seq_off = (int32_t)L.seq_off();
   mp.seg_off = (int32_t)L.seg_off();

@@ -52,7 +52,6 @@ struct hpc_plan_s {
   int32_t host_num_segs = -1;
   int32_t static_kv_heads = 0;   // static plans: grid.y
   int32_t units = 1;             // units per tile of the current work list
-  int32_t* d_cnt = nullptr;      // per-sequence arrival counters (in-kernel merge)
   int32_t* d_words = nullptr;    // plan buffer
   int32_t* h_pinned = nullptr;   // staging for hpc_decode_plan_update
   cudaEvent_t copy_done = nullptr;  // last upload from h_pinned
@@ -94,10 +93,6 @@ struct AttnParams {
   float* ws_l;                  // [cap_segs][H_q]
   int32_t* err;
   unsigned long long timeout_ns;
-  // in-kernel merge of short split sequences: per-sequence arrival counters
-  // (zero between steps; null disables) and the largest segment count merged
-  int32_t* seq_cnt;
-  int32_t fuse_merge_max;
 };
 
 struct MergeParams {
@@ -112,7 +107,6 @@ struct MergeParams {
   const float* ws_o;
   const float* ws_m;
   const float* ws_l;
-  int32_t fused_max;  // sequences with 2..fused_max segments were merged in-kernel
 };
 
 // Parameter block of the fused prologue kernel (prologue_kernel.cu).
@@ -187,9 +181,6 @@ __host__ __device__ inline WarpLayout warp_layout(int h_count, int q_len, int nc
   wl.tph = (nc / hpass) / q_len;
   return wl;
 }
-// Split sequences with at most this many segments are merged inside the
-// attention kernel by the CTA that finishes the last of them.
-constexpr int32_t kFuseMergeMax = 4;
 // Largest batch the attention kernel can plan by itself (prefix arrays in
 // shared memory next to the K/V ring).
 constexpr int32_t kFusedPlanMaxSeqs = 3072;

@@ -50,7 +50,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   const int s0 = p.plan[p.seq_off + b], s1 = p.plan[p.seq_off + b + 1];
   const int ns = s1 - s0;
   if (ns == 1) return;  // written by the attention kernel
-  if (ns >= 2 && ns <= p.fused_max) return;  // merged inside the attention kernel
   __nv_bfloat16* o = p.out + (int64_t)b * p.o_sb + (int64_t)t * p.o_st + (int64_t)j * p.o_sh +
                      4 * lane;
   float* lse = p.lse ? p.lse + (int64_t)b * p.l_sb + (int64_t)t * p.l_st + (int64_t)j * p.l_sh

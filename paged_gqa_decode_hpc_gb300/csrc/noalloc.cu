@@ -27,8 +27,7 @@ constexpr size_t kPlanBytes = round256(
     (size_t)(((kHeaderWords + kNaMaxCtas + 1 + 2 * (kNaMaxSeqs + 1)) + 3) / 4 * 4 +
              4 * (kNaMaxSeqs + kNaMaxCtas)) * sizeof(int32_t));
 constexpr size_t kErrOff = kPlanBytes;
-constexpr size_t kCntOff = kErrOff + 256;  // per-sequence merge counters
-constexpr size_t kWsOff = kCntOff + round256((size_t)kNaMaxSeqs * sizeof(int32_t));
+constexpr size_t kWsOff = kErrOff + 256;
 constexpr size_t kWsBytes =
     (size_t)(kNaMaxSeqs + kNaMaxCtas) * kNaMaxHeads * (kHeadDim + 2) * sizeof(float);
 constexpr size_t kScratchBytes = kWsOff + kWsBytes;
@@ -98,9 +97,6 @@ extern "C" hpc_status hpc_decode_attn_noalloc(const hpc_tensor* q, const hpc_ten
     base = static_cast<unsigned char*>(g_scratch_ptr[dev]);
   }
   cudaStream_t s = (cudaStream_t)stream;
-  // merge counters start every call at zero (they also reset themselves)
-  if (cudaMemsetAsync(base + kCntOff, 0, (size_t)kNaMaxSeqs * sizeof(int32_t), s) != cudaSuccess)
-    return na_fail(HPC_ERR_CUDA, "hpc_decode_attn_noalloc: clearing the merge counters failed");
   int32_t* err = device_error;
   if (!err) {
     err = reinterpret_cast<int32_t*>(base + kErrOff);
@@ -120,7 +116,6 @@ extern "C" hpc_status hpc_decode_attn_noalloc(const hpc_tensor* q, const hpc_ten
   plan.d_words = reinterpret_cast<int32_t*>(base);
   plan.d_err = err;
   plan.d_ws = reinterpret_cast<float*>(base + kWsOff);
-  plan.d_cnt = reinterpret_cast<int32_t*>(base + kCntOff);
   plan.ws_heads = kNaMaxHeads;
   if ((size_t)plan.layout.words() * sizeof(int32_t) > kPlanBytes)
     return na_fail(HPC_ERR_UNSUPPORTED, "hpc_decode_attn_noalloc: internal scratch layout error");
