@@ -687,7 +687,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // ------------------------------------------------------------ producer
     const uint64_t policy = evict_first_policy();
     uint32_t g = 0, issued = 0;
-    bool stop = false;
+    bool stop = p.withhold_copies != 0;  // failure-path test: no copy is issued
     SegCursor sc = cur0;
     int b, tb, te, slot;
     bool whole;
@@ -756,8 +756,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
       }
     }
-    if (lane == 0 && stop) {
-      // Aborting: wait (bounded) for this CTA's own copies still in flight.
+    // Every warp of the CTA meets here before any thread leaves. If a wait gave
+    // up anywhere (producer or consumer, before or after the producer finished
+    // issuing), copies may still be landing in shared memory: wait (bounded)
+    // for the last issued ones, so the CTA never exits with a copy in flight.
+    named_bar_sync(3, (NC + 1) * 32);
+    if (lane == 0 && *abort_flag) {
       for (uint32_t u = issued > (uint32_t)STAGES ? issued - STAGES : 0; u < issued; ++u)
         wait_phase(bar_full + 8 * (u % STAGES), (u / STAGES) & 1u, abort_flag, p.err,
                    1000000000ull, false);
@@ -895,6 +899,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       }
     }
   }
+  named_bar_sync(3, (NC + 1) * 32);  // see the producer's exit
   (void)c;
 }
 

@@ -40,6 +40,18 @@ unsigned long long wait_limit_ns() {
   return v;
 }
 
+// Failure-path test switch: with HPC_DECODE_TEST_WITHHOLD_COPIES=1 the
+// attention kernel's producer issues no copies, so every consumer wait runs
+// out (bounded by HPC_DECODE_WAIT_LIMIT_MS) and the step must come back with
+// HPC_DEVCHK_TIMEOUT and a usable context. Read once per process.
+bool withhold_copies() {
+  static const bool v = [] {
+    const char* s = std::getenv("HPC_DECODE_TEST_WITHHOLD_COPIES");
+    return s && s[0] == '1';
+  }();
+  return v;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
@@ -589,6 +601,7 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     p.ws_l = p.ws_m + cs * T * Hq;
     p.err = plan->d_err;
     p.timeout_ns = wait_limit_ns();
+    p.withhold_copies = withhold_copies();
     if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
     cudaError_t ce = launch_attention(p, tk, tv, fp8, gx, gy, s);
     if (ce != cudaSuccess)

@@ -93,6 +93,7 @@ struct AttnParams {
   float* ws_l;                  // [cap_segs][H_q]
   int32_t* err;
   unsigned long long timeout_ns;
+  int32_t withhold_copies;      // failure-path test: the producer issues nothing
 };
 
 struct MergeParams {

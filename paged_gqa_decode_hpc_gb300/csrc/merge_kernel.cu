@@ -11,8 +11,9 @@
 //
 // One CTA of 4 warps per (sequence, query head). A warp takes every 4th
 // partial; per round of up to 32 partials each lane loads one partial's
-// (m, l) while the o rows are fetched in batches of 8 (each lane owns 4 of the
-// 128 columns), so a round costs about two memory round trips. The warps'
+// (m, l) while the first 16 o rows are fetched alongside (each lane owns 4 of
+// the 128 columns), so a round of up to 16 partials costs one memory round
+// trip and a full round two. The warps'
 // running (M, l, o) states are combined in shared memory. A sequence with no
 // tiles gets out = 0 and lse = -inf here; a sequence finished inside one CTA
 // is skipped.
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // this warp's partials: s0 + warp + kMergeWarps * t, t = 0, 1, ...
   const int mine = (ns - warp + kMergeWarps - 1) / kMergeWarps;
+  constexpr int kBatch = 16;  // partial rows in flight per lane
   for (int r0 = 0; r0 < mine; r0 += 32) {
     const int cnt = mine - r0 < 32 ? mine - r0 : 32;
     const int64_t my_s = s0 + warp + (int64_t)kMergeWarps * (r0 + lane);
@@ -75,6 +77,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
       mk = p.ws_m[my_s * hq + jv];
       lk = p.ws_l[my_s * hq + jv];
     }
+    // the first rows do not depend on the weights: fetch them with (m, l)
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int64_t sr = s0 + warp + (int64_t)kMergeWarps * (r0 + u);
+      v[u] = u < cnt ? *reinterpret_cast<const float4*>(obase + sr * hq * kHeadDim)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const float Mn = fmaxf(M, warp_max(mk));
     if (Mn == -INFINITY) continue;  // only empty partials so far
     const float scale = M == -INFINITY ? 0.f : ptx_ex2(M - Mn);
@@ -82,16 +92,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     L = L * scale + warp_sum(lk * wk);
     acc.x *= scale; acc.y *= scale; acc.z *= scale; acc.w *= scale;
     M = Mn;
-    for (int k0 = 0; k0 < cnt; k0 += 8) {
-      float4 v[8];
+    for (int k0 = 0; k0 < cnt; k0 += kBatch) {
+      if (k0 > 0) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int64_t s = s0 + warp + (int64_t)kMergeWarps * (r0 + k0 + u);
-        v[u] = k0 + u < cnt ? *reinterpret_cast<const float4*>(obase + s * hq * kHeadDim)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kBatch; ++u) {
+          const int64_t sr = s0 + warp + (int64_t)kMergeWarps * (r0 + k0 + u);
+          v[u] = k0 + u < cnt ? *reinterpret_cast<const float4*>(obase + sr * hq * kHeadDim)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const float w = __shfl_sync(0xffffffffu, wk, (k0 + u) & 31);
         acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
       }

@@ -1,0 +1,83 @@
+"""Failure detection on the GPU without a fault: the attention kernel's
+bounded waits must end a step whose data never arrives with an error status,
+and leave the context usable.
+
+A child process sets HPC_DECODE_TEST_WITHHOLD_COPIES=1 (the producer warp
+issues no copies, so every consumer waits on a word nothing sets) and a
+200 ms wait limit, runs one step, and reports the device-check bits, the
+time the step took and whether CUDA still works afterwards. No trap, no bad
+address, no endless loop is involved."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_hpc_gb300 as hpc
+from paged_gqa_decode_hpc_gb300 import workloads as W
+from tests.gpu_util import assert_parity, device_workload
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import torch
+import paged_gqa_decode_hpc_gb300 as hpc
+from paged_gqa_decode_hpc_gb300 import workloads as W
+from tests.gpu_util import device_workload
+hpc.load_library()
+res = {}
+for hkv, hq in ((8, 64), (1, 8)):  # without and with the warps' combine step
+    w = W.make_workload(W.Config(99, "fail", hq, hkv, "bf16"), lengths=[3000, 64, 700], seed=71)
+    d = device_workload(w)
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(3, sms, hq)
+    out = torch.zeros(w.q.shape, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.time()
+    hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out)
+    bits = hpc.hpc_decode_plan_status(plan)  # synchronises
+    res[str(hkv)] = {"bits": bits, "seconds": time.time() - t0}
+    plan.destroy()
+# the context still works
+res["usable"] = float(torch.arange(1000, device="cuda", dtype=torch.float32).sum().item()) == 499500.0
+print(json.dumps(res))
+"""
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    hpc.load_library()
+
+
+def test_withheld_copies_end_in_a_timeout_status_and_a_usable_context():
+    env = dict(os.environ, HPC_DECODE_TEST_WITHHOLD_COPIES="1", HPC_DECODE_WAIT_LIMIT_MS="200")
+    r = subprocess.run([sys.executable, "-c", CHILD, ROOT], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    for hkv in ("8", "1"):
+        assert res[hkv]["bits"] & hpc.HPC_DEVCHK_TIMEOUT, res
+        assert res[hkv]["seconds"] < 30, res
+    assert res["usable"]
+    # and this process, without the switch, still computes the right answer
+    w = W.make_workload(W.Config(99, "fail", 64, 8, "bf16"), lengths=[3000, 64, 700], seed=71)
+    d = device_workload(w)
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(3, sms, 64)
+    out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out, lse)
+    assert hpc.hpc_decode_plan_status(plan) == 0
+    plan.destroy()
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse)
