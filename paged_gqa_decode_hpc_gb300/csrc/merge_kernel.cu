@@ -11,9 +11,10 @@
 //
 // One CTA of 4 warps per (sequence, query head). A warp takes every 4th
 // partial; per round of up to 32 partials each lane loads one partial's
-// (m, l) while the first 16 o rows are fetched alongside (each lane owns 4 of
-// the 128 columns), so a round of up to 16 partials costs one memory round
-// trip and a full round two. The warps'
+// (m, l) while the first 8 o rows are fetched alongside (each lane owns 4 of
+// the 128 columns), so a round of up to 8 partials costs one memory round
+// trip. At 64 registers, 8 CTAs fit on an SM: batches with many short split
+// sequences (thousands of CTAs) take fewer waves. The warps'
 // running (M, l, o) states are combined in shared memory. A sequence with no
 // tiles gets out = 0 and lse = -inf here; a sequence finished inside one CTA
 // is skipped.
@@ -40,7 +41,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32, 8) merge_kernel(const MergeParams p) {
   __shared__ float4 s_o[kMergeWarps][32];
   __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
   griddep_wait();  // partials come from the attention kernel
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   // this warp's partials: s0 + warp + kMergeWarps * t, t = 0, 1, ...
   const int mine = (ns - warp + kMergeWarps - 1) / kMergeWarps;
-  constexpr int kBatch = 16;  // partial rows in flight per lane
+  constexpr int kBatch = 8;  // partial rows in flight per lane
   for (int r0 = 0; r0 < mine; r0 += 32) {
     const int cnt = mine - r0 < 32 ? mine - r0 : 32;
     const int64_t my_s = s0 + warp + (int64_t)kMergeWarps * (r0 + lane);
