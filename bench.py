@@ -464,22 +464,33 @@ def run_hpc(args, ws, rank, local):
 
     # ---- end to end through the public API, host buffers
     if not args.no_e2e:
-        q_h = w.q.pin_memory()
-        sl_h = w.seq_lens.pin_memory()
-        bt_h = w.block_table.pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        h2d = q_h.numel() * 2 + sl_h.numel() * 4 + bt_h.numel() * 4
-        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        # One pinned staging buffer per direction (q | lengths | block table
+        # up, out | lse down), so a step costs one copy each way.
+        def packed(parts, device):
+            offs, n = [], 0
+            for t in parts:
+                offs.append(n)
+                n += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.empty(n, dtype=torch.uint8, device=device,
+                              pin_memory=(device == "cpu"))
+            views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                     for o, t in zip(offs, parts)]
+            return buf, views
+        h_in, (q_h, sl_h, bt_h) = packed([w.q, w.seq_lens, w.block_table], "cpu")
+        q_h.copy_(w.q)
+        sl_h.copy_(w.seq_lens)
+        bt_h.copy_(w.block_table)
+        d_in, (q_e, sl_e, bt_e) = packed([w.q, w.seq_lens, w.block_table], dev)
+        d_out, (out_e, lse_e) = packed([out, lse], dev)
+        h_out, (out_h, lse_h) = packed([out, lse], "cpu")
+        h2d = h_in.numel()
+        d2h = h_out.numel()
 
         def e2e_step():
-            q.copy_(q_h, non_blocking=True)
-            sl.copy_(sl_h, non_blocking=True)
-            bt.copy_(bt_h, non_blocking=True)
-            hpc.hpc_decode_step(q, kc, vc, bt, sl, plan, num_sms, out, lse, stream=stream,
-                                k_scale=w.k_scale, v_scale=w.v_scale)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            hpc.hpc_decode_step(q_e, kc, vc, bt_e, sl_e, plan, num_sms, out_e, lse_e,
+                                stream=stream, k_scale=w.k_scale, v_scale=w.v_scale)
+            h_out.copy_(d_out, non_blocking=True)
 
         for _ in range(max(3, args.warmup)):
             flush_l2()
@@ -495,9 +506,15 @@ def run_hpc(args, ws, rank, local):
         torch.cuda.synchronize()
         barrier(ws)
         e2e_ms = max_over_ranks(ws, statistics.mean(a.elapsed_time(b) for a, b in es))
+        # the host copy of the result must equal a device-resident step's
+        hpc.hpc_decode_step(q, kc, vc, bt, sl, plan, num_sms, out, lse, stream=stream,
+                            k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        same = bool(torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu()))
         line["e2e"] = {"value": round(ws * nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                        "us_per_step": round(e2e_ms * 1e3, 2),
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "result_matches_device_step": same}
         line["gpu_launches"] += launches_per_step * args.steps
 
     # ---- fp64 CPU oracle on host cores (rank 0, N = 1 only)
