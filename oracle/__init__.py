@@ -7,7 +7,9 @@ anything here, and nothing here imports the CUDA library: the two share no
 code. Only the seeded input generators are common to both sides.
 
 Contents:
-  decode_ref.c   fp64 paged GQA decode from its definition (POSIX threads).
+  decode_ref.c   fp64 paged GQA decode from its definition (POSIX threads);
+                 __init__.py reduces multi-token decode and ragged prefill /
+                 extend to it, one (sequence, new token) at a time.
   plan_ref.py    the dynamic (load-balanced) and static split-KV tile plans.
   merge_ref.py   partial softmax states and their log-sum-exp merge.
 
@@ -165,3 +167,44 @@ def paged_decode_multi(q, k_cache, v_cache, block_table, seq_lens, *, num_kv_hea
                             softmax_scale=softmax_scale, kv_is_fp8=kv_is_fp8, k_scale=k_scale,
                             v_scale=v_scale, num_threads=num_threads, lib=lib)
     return out.reshape(B, T, qt.shape[2], -1), lse.reshape(B, T, -1)
+
+
+def paged_extend(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, *, num_kv_heads: int,
+                 softmax_scale: float, kv_is_fp8: bool = False, k_scale: float = 1.0,
+                 v_scale: float = 1.0, num_threads: int = 0, lib=None):
+    """Prefill / extend attention over the paged cache ("vLLM x HPC-Ops",
+    section "Attention Across Prefill, Extend and Decode Shapes"), by its
+    definition. Sequence b brings n_b = cu_q_lens[b+1] - cu_q_lens[b] new
+    tokens, already written to its cache, so they are its last n_b positions
+    of L_b = seq_lens[b]; new token i (0-based) attends causally to the
+    positions before L_b - n_b + 1 + i. Prefill is the case n_b = L_b.
+    Each (sequence, new token) is a plain decode of that length over the
+    sequence's block table, computed by the fp64 decode oracle.
+
+    q: bf16 [total_q][H_q][D] (rows of sequence b at cu_q_lens[b]..);
+    cu_q_lens int32 [B+1], non-decreasing from 0 to total_q.
+    Returns (out [total_q][H_q][D] f64, lse [total_q][H_q] f64).
+    """
+    qt = q if hasattr(q, "shape") else np.asarray(q)
+    cu = _as_np(cu_q_lens, np.int32).astype(np.int64)
+    lens = _as_np(seq_lens, np.int32)
+    bt = _as_np(block_table, np.int32)
+    B = int(lens.shape[0])
+    total = int(qt.shape[0])
+    if cu.shape != (B + 1,) or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_q_lens must run from 0 to total_q without decreasing")
+    rows, vlen = [], []
+    for b in range(B):
+        n = int(cu[b + 1] - cu[b])
+        if n > int(lens[b]):
+            raise ValueError("a sequence has more new tokens than positions")
+        for i in range(n):
+            rows.append(b)
+            vlen.append(int(lens[b]) - n + 1 + i)
+    if total == 0:
+        return (np.zeros((0,) + tuple(qt.shape[1:]), dtype=np.float64),
+                np.zeros((0, qt.shape[1]), dtype=np.float64))
+    return paged_decode(qt, k_cache, v_cache, bt[np.array(rows, dtype=np.int64)],
+                        np.array(vlen, dtype=np.int32), num_kv_heads=num_kv_heads,
+                        softmax_scale=softmax_scale, kv_is_fp8=kv_is_fp8, k_scale=k_scale,
+                        v_scale=v_scale, num_threads=num_threads, lib=lib)

@@ -200,3 +200,20 @@ def make_multi_query(w: Workload, q_len: int, seed: int, q_scale: float = 1.0) -
     gen = torch.Generator().manual_seed(seed)
     return (torch.randn(w.num_seqs, q_len, w.num_q_heads, HEAD_DIM, generator=gen)
             * q_scale).to(torch.bfloat16)
+
+
+def make_extend_query(w: Workload, q_lens: List[int], seed: int, q_scale: float = 1.0):
+    """Seeded N(0,1) queries of q_lens[b] new tokens of each sequence, packed
+    ragged: (q bf16 [total_q][H_q][D], cu_q_lens int32 [B+1]). The new tokens
+    are the last q_lens[b] positions of sequence b (q_lens[b] <= its length)."""
+    if len(q_lens) != w.num_seqs:
+        raise ValueError("one q_len per sequence")
+    for n, L in zip(q_lens, w.seq_lens.tolist()):
+        if n < 0 or n > L:
+            raise ValueError("q_len must lie in [0, seq_len]")
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + int(n))
+    gen = torch.Generator().manual_seed(seed)
+    q = (torch.randn(cu[-1], w.num_q_heads, HEAD_DIM, generator=gen) * q_scale).to(torch.bfloat16)
+    return q, torch.tensor(cu, dtype=torch.int32)
