@@ -347,6 +347,38 @@ hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in
                                   hpc_tensor* q_out, hpc_tensor* q_out_fp8, hpc_tensor* k_cache,
                                   hpc_tensor* v_cache, int32_t* device_error, void* stream);
 
+/*
+ * hpc_extend_attn -- prefill / extend attention over the paged cache ("vLLM x
+ * HPC-Ops", section "Attention Across Prefill, Extend and Decode Shapes",
+ * which benchmarks q512 prefill with the decode kernel's shapes). Sequence b
+ * has n_b = cu_q_lens[b+1] - cu_q_lens[b] new tokens whose K and V are
+ * already in its cache as its last n_b positions of L_b = seq_lens[b]; new
+ * token i attends to positions 0 .. L_b - n_b + i (causal). Prefill is
+ * n_b = L_b, decode n_b = 1. Runs on the tcgen05 tensor cores, one CTA per
+ * (KV head, 16 new tokens of one sequence).
+ *   q           device bf16 [total_q][H_q][128], ragged: the rows of sequence
+ *               b start at cu_q_lens[b]; innermost stride 1, other strides
+ *               multiples of 8 elements, base 16-byte aligned
+ *   k_cache, v_cache, block_table: as hpc_decode_attn, but bf16 only (an
+ *               fp8_e4m3 cache gives HPC_ERR_UNSUPPORTED)
+ *   seq_lens    device int32 [B], L_b >= n_b (else HPC_DEVCHK_BAD_LENGTH and
+ *               that sequence's rows are not written)
+ *   cu_q_lens   device int32 [B+1], non-decreasing, cu_q_lens[0] = 0,
+ *               cu_q_lens[B] = total_q
+ *   out         device bf16 [total_q][H_q][128] (written), q's layout rules
+ *   lse         device f32 [total_q][H_q] natural-log LSE (written), or NULL
+ *   softmax_scale  > 0, or <= 0 for 1/sqrt(128)
+ *   device_error   optional device int32 receiving HPC_DEVCHK_* bits
+ * Requirements: H_q == 8 * H_kv, head_dim 128, 64-token blocks, at most
+ * 65535 - B 16-token tiles per call (else HPC_ERR_UNSUPPORTED). Allocates
+ * nothing; never synchronises the stream.
+ */
+hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
+                           const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                           const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
+                           hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
+                           int32_t* device_error, void* stream);
+
 /* hpc_device_sm_count -- streaming multiprocessors of the current device. */
 hpc_status hpc_device_sm_count(int32_t* num_sms);
 

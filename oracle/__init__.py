@@ -171,7 +171,7 @@ def paged_decode_multi(q, k_cache, v_cache, block_table, seq_lens, *, num_kv_hea
 
 def paged_extend(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, *, num_kv_heads: int,
                  softmax_scale: float, kv_is_fp8: bool = False, k_scale: float = 1.0,
-                 v_scale: float = 1.0, num_threads: int = 0, lib=None):
+                 v_scale: float = 1.0, num_threads: int = 0, lib=None, rows=None):
     """Prefill / extend attention over the paged cache ("vLLM x HPC-Ops",
     section "Attention Across Prefill, Extend and Decode Shapes"), by its
     definition. Sequence b brings n_b = cu_q_lens[b+1] - cu_q_lens[b] new
@@ -183,7 +183,8 @@ def paged_extend(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, *, num_k
 
     q: bf16 [total_q][H_q][D] (rows of sequence b at cu_q_lens[b]..);
     cu_q_lens int32 [B+1], non-decreasing from 0 to total_q.
-    Returns (out [total_q][H_q][D] f64, lse [total_q][H_q] f64).
+    Returns (out [total_q][H_q][D] f64, lse [total_q][H_q] f64); with `rows`
+    (indices into total_q) only those rows, in that order.
     """
     qt = q if hasattr(q, "shape") else np.asarray(q)
     cu = _as_np(cu_q_lens, np.int32).astype(np.int64)
@@ -193,18 +194,23 @@ def paged_extend(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, *, num_k
     total = int(qt.shape[0])
     if cu.shape != (B + 1,) or cu[0] != 0 or cu[-1] != total or np.any(np.diff(cu) < 0):
         raise ValueError("cu_q_lens must run from 0 to total_q without decreasing")
-    rows, vlen = [], []
+    seq_rows, vlen = [], []
     for b in range(B):
         n = int(cu[b + 1] - cu[b])
         if n > int(lens[b]):
             raise ValueError("a sequence has more new tokens than positions")
         for i in range(n):
-            rows.append(b)
+            seq_rows.append(b)
             vlen.append(int(lens[b]) - n + 1 + i)
-    if total == 0:
+    seq_of = np.array(seq_rows, dtype=np.int64)
+    vlen = np.array(vlen, dtype=np.int32)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        qt = qt[rows]
+        seq_of, vlen = seq_of[rows], vlen[rows]
+    if len(vlen) == 0:
         return (np.zeros((0,) + tuple(qt.shape[1:]), dtype=np.float64),
                 np.zeros((0, qt.shape[1]), dtype=np.float64))
-    return paged_decode(qt, k_cache, v_cache, bt[np.array(rows, dtype=np.int64)],
-                        np.array(vlen, dtype=np.int32), num_kv_heads=num_kv_heads,
+    return paged_decode(qt, k_cache, v_cache, bt[seq_of], vlen, num_kv_heads=num_kv_heads,
                         softmax_scale=softmax_scale, kv_is_fp8=kv_is_fp8, k_scale=k_scale,
                         v_scale=v_scale, num_threads=num_threads, lib=lib)

@@ -25,7 +25,7 @@ __all__ = [
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
     "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc", "hpc_decode_step",
-    "hpc_rope_norm_kv_write",
+    "hpc_rope_norm_kv_write", "hpc_extend_attn",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
 ]
@@ -105,6 +105,7 @@ def load_library():
             "hpc_decode_step": [T, T, T, T, T, P, i32, T, T, P],
             "hpc_rope_norm_kv_write": [T, T, T, T, T, T, T, ctypes.c_float, ctypes.c_float,
                                        T, T, T, T, P, P],
+            "hpc_extend_attn": [T, T, T, T, T, T, T, T, ctypes.c_float, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -332,6 +333,24 @@ def hpc_rope_norm_kv_write(q_in, k_in, v_in, seq_lens, block_table, q_norm_weigh
     _check(lib.hpc_rope_norm_kv_write(*[ref(t) for t in d], ctypes.c_float(eps),
                                       ctypes.c_float(rope_base), ref(qo), ref(qf), ref(kc),
                                       ref(vc), err, _stream_ptr(stream)))
+
+
+def hpc_extend_attn(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse=None,
+                    softmax_scale: Optional[float] = None, device_error=None, stream=None):
+    """Prefill / extend attention on the tensor cores: q and out are bf16
+    [total_q][H_q][128] with the new tokens of sequence b in rows
+    cu_q_lens[b] .. cu_q_lens[b+1]-1 (the last positions of its cache);
+    lse f32 [total_q][H_q] or None; device_error an int32 CUDA tensor
+    receiving HPC_DEVCHK_* bits, or None."""
+    lib = load_library()
+    tq, tk, tv = make_tensor(q), make_tensor(k_cache), make_tensor(v_cache)
+    tb, ts, tc = make_tensor(block_table), make_tensor(seq_lens), make_tensor(cu_q_lens)
+    to, tl = make_tensor(out), make_tensor(lse)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    err = ctypes.c_void_p(device_error.data_ptr()) if device_error is not None else None
+    _check(lib.hpc_extend_attn(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), ref(tc), ref(to),
+                               ref(tl), ctypes.c_float(softmax_scale or -1.0), err,
+                               _stream_ptr(stream)))
 
 
 def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int, out,

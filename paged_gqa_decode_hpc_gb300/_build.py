@@ -34,7 +34,7 @@ def _sources():
 
 
 def _inputs():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + \
+    return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "hpc_internal.h"
+#include "prefill.h"
 
 namespace hpc {
 
@@ -825,3 +826,134 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Prefill / extend attention (prefill_kernel.cu).
+namespace hpc {
+namespace {
+
+// 3-D TMA descriptor over q [total_q][H_q][128] bf16: box = 16 tokens x
+// 8 heads x 64 columns, 128-byte swizzle (one 16 KB half of a 128-row tile).
+hpc_status make_q_map(const hpc_tensor* q, CUtensorMap* map) {
+  auto enc = encode_fn();
+  if (!enc) return fail(HPC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)q->shape[1], (cuuint64_t)q->shape[0]};
+  cuuint64_t strides[2] = {(cuuint64_t)q->stride[1] * 2, (cuuint64_t)q->stride[0] * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kGroup, (cuuint32_t)kExtendTileTokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(HPC_ERR_INVALID_ARG,
+                "cuTensorMapEncodeTiled rejected q (error " + std::to_string((int)r) + ")");
+  return HPC_OK;
+}
+
+}  // namespace
+}  // namespace hpc
+
+extern "C" hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                      const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                      const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
+                                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
+                                      int32_t* device_error, void* stream) {
+  using namespace hpc;
+  hpc_status st;
+  if ((st = check_tensor(q, "q", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
+  if ((st = check_tensor(v_cache, "v_cache", 4)) != HPC_OK) return st;
+  if ((st = check_tensor(block_table, "block_table", 2)) != HPC_OK) return st;
+  if ((st = check_tensor(seq_lens, "seq_lens", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(cu_q_lens, "cu_q_lens", 1)) != HPC_OK) return st;
+  if ((st = check_tensor(out, "out", 3)) != HPC_OK) return st;
+  if ((st = check_tensor(lse, "lse", 2, true)) != HPC_OK) return st;
+  const bool has_lse = lse && lse->data;
+  const int64_t total_q = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t B = seq_lens->shape[0];
+  const int64_t NB = k_cache->shape[0], Hkv = k_cache->shape[1];
+  if (q->dtype != HPC_BF16 || out->dtype != HPC_BF16)
+    return fail(HPC_ERR_INVALID_ARG, "q and out must be bf16");
+  if (k_cache->dtype != v_cache->dtype ||
+      (k_cache->dtype != HPC_BF16 && k_cache->dtype != HPC_FP8_E4M3))
+    return fail(HPC_ERR_INVALID_ARG, "k_cache/v_cache must both be bf16 or both fp8_e4m3");
+  if (k_cache->dtype != HPC_BF16)
+    return fail(HPC_ERR_UNSUPPORTED, "prefill / extend attention reads a bf16 cache only");
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i] || k_cache->stride[i] != v_cache->stride[i])
+      return fail(HPC_ERR_INVALID_ARG, "k_cache and v_cache must have the same shape and strides");
+  if (D != kHeadDim || k_cache->shape[3] != kHeadDim)
+    return fail(HPC_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (k_cache->shape[2] != kBlockTokens)
+    return fail(HPC_ERR_UNSUPPORTED, "KV blocks must hold 64 tokens");
+  if (Hkv <= 0 || Hq != kGroup * Hkv)
+    return fail(HPC_ERR_UNSUPPORTED, "num_q_heads must be 8 * num_kv_heads");
+  for (int i = 0; i < 3; ++i)
+    if (out->shape[i] != q->shape[i]) return fail(HPC_ERR_INVALID_ARG, "out must have q's shape");
+  if (has_lse && (lse->dtype != HPC_F32 || lse->shape[0] != total_q || lse->shape[1] != Hq))
+    return fail(HPC_ERR_INVALID_ARG, "lse must be f32 [total_q][H_q]");
+  if (block_table->dtype != HPC_I32 || block_table->shape[0] != B || block_table->stride[1] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "block_table must be int32 [B][max_blocks], row-contiguous");
+  if (seq_lens->dtype != HPC_I32 || (B > 1 && seq_lens->stride[0] != 1))
+    return fail(HPC_ERR_INVALID_ARG, "seq_lens must be contiguous int32 [B]");
+  if (cu_q_lens->dtype != HPC_I32 || cu_q_lens->shape[0] != B + 1 || cu_q_lens->stride[0] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "cu_q_lens must be contiguous int32 [B+1]");
+  if (q->stride[2] != 1 || out->stride[2] != 1 || k_cache->stride[3] != 1)
+    return fail(HPC_ERR_INVALID_ARG, "innermost stride of q, out and the caches must be 1");
+  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+      !aligned(q->data, 16) || !aligned(out->data, 16))
+    return fail(HPC_ERR_INVALID_ARG, "q/out must be 16-byte aligned with strides of 8 elements");
+  for (int i = 0; i < 3; ++i)
+    if ((k_cache->stride[i] * 2) % 16)
+      return fail(HPC_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
+  if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
+    return fail(HPC_ERR_INVALID_ARG, "cache base addresses must be 16-byte aligned");
+  const int64_t s_head = k_cache->stride[1], s_slot = k_cache->stride[2],
+                s_blk = k_cache->stride[0];
+  bool swap;
+  if (s_slot >= kHeadDim && s_head >= kBlockTokens * s_slot && s_blk >= Hkv * s_head)
+    swap = false;
+  else if (s_head >= kHeadDim && s_slot >= Hkv * s_head && s_blk >= kBlockTokens * s_slot)
+    swap = true;
+  else
+    return fail(HPC_ERR_UNSUPPORTED, "cache strides must describe a [blocks][kv heads][64][128] "
+                                     "or [blocks][64][kv heads][128] layout");
+  if (B == 0 || total_q == 0) return HPC_OK;
+  if (NB == 0) return fail(HPC_ERR_INVALID_ARG, "k_cache has no blocks");
+  if (B > INT32_MAX || total_q > INT32_MAX || NB > INT32_MAX || block_table->shape[1] > INT32_MAX)
+    return fail(HPC_ERR_INVALID_ARG, "sizes exceed int32");
+  // 16-token tiles: sum_b ceil(n_b / 16) <= total_q / 16 + B
+  const int64_t tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + B;
+  if (tiles > 65535)
+    return fail(HPC_ERR_UNSUPPORTED, "too many 16-token tiles in one call (split the batch)");
+  CUtensorMap tq, tk, tv;
+  if ((st = make_q_map(q, &tq)) != HPC_OK) return st;
+  if ((st = make_kv_map(k_cache, false, swap, &tk)) != HPC_OK) return st;
+  if ((st = make_kv_map(v_cache, false, swap, &tv)) != HPC_OK) return st;
+  ExtendParams p;
+  std::memset(&p, 0, sizeof p);
+  p.block_table = (const int32_t*)block_table->data;
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = (int32_t)block_table->shape[1];
+  p.seq_lens = (const int32_t*)seq_lens->data;
+  p.cu_q_lens = (const int32_t*)cu_q_lens->data;
+  p.num_seqs = (int32_t)B;
+  p.num_q_heads = (int32_t)Hq;
+  p.num_kv_heads = (int32_t)Hkv;
+  p.num_blocks = (int32_t)NB;
+  p.kv_swap = swap;
+  p.out = (__nv_bfloat16*)out->data;
+  p.o_st = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.lse = has_lse ? (float*)lse->data : nullptr;
+  p.l_st = has_lse ? lse->stride[0] : 0;
+  p.l_sh = has_lse ? lse->stride[1] : 0;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p.score_scale_log2 = scale * 1.4426950408889634f;
+  p.err = device_error;
+  p.timeout_ns = wait_limit_ns();
+  cudaError_t e = launch_extend(p, tq, tk, tv, (int)tiles, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(HPC_ERR_CUDA, std::string("extend launch: ") + cudaGetErrorString(e));
+  return HPC_OK;
+}

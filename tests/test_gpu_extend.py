@@ -1,0 +1,156 @@
+"""GPU parity of prefill / extend attention (hpc_extend_attn, the tcgen05
+kernel) against the fp64 oracle: ragged batches, prefill from an empty
+cache, extends over long contexts, sharp softmax, block-permutation and
+cache-layout invariance, sampled rows of a large prefill, and the argument
+and device checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_hpc_gb300 as hpc
+from paged_gqa_decode_hpc_gb300 import workloads as W
+from tests.gpu_util import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    hpc.load_library()
+
+
+def _cfg(hq, hkv):
+    return W.Config(95, "extend", hq, hkv, "bf16")
+
+
+def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err=0):
+    dev = "cuda"
+    qd = q.to(dev)
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    hpc.hpc_extend_attn(qd, w.k_cache.to(dev) if k is None else k,
+                        w.v_cache.to(dev) if v is None else v,
+                        w.block_table.to(dev) if bt is None else bt, w.seq_lens.to(dev),
+                        cu.to(dev), out, lse, softmax_scale=softmax_scale, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == expect_err, f"device check bits {int(err.item())}"
+    return out, lse
+
+
+def _oracle(w, q, cu, rows=None, softmax_scale=None):
+    return oracle.paged_extend(q, w.k_cache, w.v_cache, w.block_table, w.seq_lens, cu,
+                               num_kv_heads=w.num_kv_heads,
+                               softmax_scale=softmax_scale or w.softmax_scale, rows=rows)
+
+
+CASES = [
+    # (H_q, H_kv, lengths, new tokens per sequence)
+    (8, 1, [64], [64]),                                   # one prefill tile row block
+    (16, 2, [100], [100]),                                # prefill with a ragged tail
+    (64, 8, [512], [512]),                                # q512 prefill
+    (64, 8, [70, 9, 130, 64, 1000], [70, 3, 66, 1, 17]),  # ragged mix of prefill / extend
+    (64, 8, [4096], [100]),                               # extend over a long context
+    (32, 4, [50, 300, 17], [0, 20, 17]),                  # a sequence with no new token
+    (128, 16, [200, 65], [33, 65]),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,lens,qn", CASES)
+def test_matches_oracle(hq, hkv, lens, qn):
+    w = W.make_workload(_cfg(hq, hkv), lengths=lens, seed=40 + len(lens))
+    q, cu = W.make_extend_query(w, qn, seed=41)
+    out, lse = run_extend(w, q, cu)
+    ref_out, ref_lse = _oracle(w, q, cu)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                  label=f"extend {lens} {qn}")
+
+
+def test_sharp_softmax_and_explicit_scale():
+    # q x 8 makes the softmax peaked, so row maxima jump between tiles and the
+    # O rescale path runs; a second scale checks the scale argument
+    w = W.make_workload(_cfg(64, 8), lengths=[700, 129], seed=42)
+    q, cu = W.make_extend_query(w, [300, 129], seed=43, q_scale=8.0)
+    for scale in (None, 0.05):
+        out, lse = run_extend(w, q, cu, softmax_scale=scale)
+        ref_out, ref_lse = _oracle(w, q, cu, softmax_scale=scale)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      label=f"sharp scale={scale}")
+
+
+def test_block_permutation_and_layout_invariance():
+    w = W.make_workload(_cfg(64, 8), lengths=[300, 77], seed=44, slack_blocks=5)
+    q, cu = W.make_extend_query(w, [120, 40], seed=45)
+    out1, lse1 = run_extend(w, q, cu)
+    # same logical cache under another physical placement
+    nb = w.k_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(46))
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt2 = torch.where(w.block_table >= 0, perm[w.block_table.clamp(min=0).long()].int(),
+                      w.block_table)
+    out2, lse2 = run_extend(w, q, cu, k=k2.cuda(), v=v2.cuda(), bt=bt2.cuda())
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    # [blocks][64][kv heads][128] storage passed as a permuted view
+    ks = w.k_cache.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    vs = w.v_cache.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3)
+    out3, lse3 = run_extend(w, q, cu, k=ks, v=vs)
+    assert torch.equal(out1, out3) and torch.equal(lse1, lse3)
+
+
+def test_large_prefill_sampled_rows():
+    # 4 x 4096-token prefill at the decode configs' head shape: every row finite,
+    # 64 sampled rows (first, last and tile edges included) against the oracle
+    lens = [4096] * 4
+    w = W.make_workload(_cfg(64, 8), lengths=lens, seed=47)
+    q, cu = W.make_extend_query(w, lens, seed=48)
+    out, lse = run_extend(w, q, cu)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    g = torch.Generator().manual_seed(49)
+    rows = sorted(set([0, 15, 16, 4095, 4096, 8191, 12287, 16383] +
+                      torch.randint(0, 16384, (56,), generator=g).tolist()))
+    ref_out, ref_lse = _oracle(w, q, cu, rows=rows)
+    assert_parity(out[rows].double().cpu().numpy(), lse[rows].double().cpu().numpy(), ref_out,
+                  ref_lse, label="prefill 4 x 4096 sampled")
+
+
+def test_decode_shape_equals_decode_kernel():
+    # one new token per sequence is a decode: same answer as the decode path
+    w = W.make_workload(_cfg(64, 8), lengths=[1, 64, 65, 3000], seed=50)
+    cu = torch.arange(5, dtype=torch.int32)
+    out, lse = run_extend(w, w.q, cu)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                  label="extend as decode")
+
+
+def test_argument_and_device_checks():
+    w = W.make_workload(_cfg(16, 2), lengths=[40, 80], seed=51)
+    q, cu = W.make_extend_query(w, [10, 20], seed=52)
+    dev = "cuda"
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    args = [q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_table.to(dev),
+            w.seq_lens.to(dev), cu.to(dev), out]
+    # an fp8 cache is not supported by this kernel
+    k8 = torch.zeros(w.k_cache.shape, dtype=torch.uint8, device=dev)
+    with pytest.raises(hpc.HpcError) as e:
+        hpc.hpc_extend_attn(args[0], k8, k8, *args[3:])
+    assert e.value.status == hpc.HPC_ERR_UNSUPPORTED
+    # cu_q_lens of the wrong length
+    with pytest.raises(hpc.HpcError) as e:
+        hpc.hpc_extend_attn(*args[:5], cu[:2].to(dev), out)
+    assert e.value.status == hpc.HPC_ERR_INVALID_ARG
+    # more new tokens than positions: flagged on the device, rows left alone
+    sl = torch.tensor([40, 15], dtype=torch.int32)
+    w_bad = W.Workload(w.config_name, sl, w.block_table, w.q, w.k_cache, w.v_cache, 1.0, 1.0,
+                       "bf16", w.softmax_scale, 16, 2)
+    run_extend(w_bad, q, cu, expect_err=hpc.HPC_DEVCHK_BAD_LENGTH)
+    # a block id out of range reads zeros and is flagged
+    bt = w.block_table.clone()
+    bt[1, 0] = 10_000
+    run_extend(w, q, cu, bt=bt.to(dev), expect_err=hpc.HPC_DEVCHK_BAD_BLOCK)

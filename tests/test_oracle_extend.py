@@ -108,3 +108,13 @@ def test_rejects_bad_cu_q_lens():
         _extend(w, q, torch.tensor([0, 2, 8], dtype=torch.int32))   # 6 new tokens > 5 positions
     with pytest.raises(ValueError):
         _extend(w, q, torch.tensor([0, 5, 4], dtype=torch.int32))
+
+
+def test_row_subset_equals_full_rows():
+    w = W.make_workload(_cfg(16, 2), lengths=[90, 200], seed=30)
+    q, cu = W.make_extend_query(w, [40, 70], seed=31)
+    out, lse = _extend(w, q, cu)
+    rows = [0, 39, 40, 77, 109]
+    so, sl = oracle.paged_extend(q, w.k_cache, w.v_cache, w.block_table, w.seq_lens, cu,
+                                 num_kv_heads=2, softmax_scale=w.softmax_scale, rows=rows)
+    assert np.array_equal(so, out[rows]) and np.array_equal(sl, lse[rows])
