@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak), mixed-length paged GQA"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 WORKLOAD_TEXT = {
     "tiny": "tiny: 4 seqs KV {37,64,200,1000}, 8 q / 1 kv heads, d128, bf16 KV",
@@ -66,6 +67,10 @@ def parse_args():
                     help="skip timing the fused prologue kernel")
     ap.add_argument("--no-copy-probe", action="store_true",
                     help="skip the device-to-device copy bandwidth probe")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill / extend (tcgen05) timings")
+    ap.add_argument("--prefill-cases", default="q512_prefill,prefill_4x4096,extend_8x(8192+512)",
+                    help="prefill / extend cases to time (comma list)")
     ap.add_argument("--scale-lengths", type=float, default=1.0,
                     help="scale every KV length of the config (smaller profiling cases)")
     return ap.parse_args()
@@ -83,6 +88,29 @@ def measured_peak_gbs():
     except Exception:
         pass
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def measured_peak_bf16_tflops():
+    """Dense bf16 tensor peak for a kernel timed alone (the burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"]), "measured burst (MEASURED_PEAKS.json)"
+    except Exception:
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s (no MEASURED_PEAKS.json)"
+
+
+def extend_flops(lens, qn, num_q_heads):
+    """Useful FLOPs of causal prefill / extend attention: per query row and
+    visible key, 2*128 for q.k and 2*128 for p*v."""
+    vis = 0
+    for L, n in zip(lens, qn):
+        # new token i sees L - n + 1 + i keys
+        vis += n * (L - n + 1) + n * (n - 1) // 2
+    return 4 * 128 * num_q_heads * vis
 
 
 def kernel_source_digest():
@@ -600,6 +628,57 @@ def run_hpc(args, ws, rank, local):
         res["note"] = "latency-bound: the bytes are small; one launch of B*(H_q+2*H_kv) warps"
         line["prologue"] = res
         del kc2, vc2
+
+    # ---- prefill / extend attention (tcgen05), the pages' prefill shapes
+    if not args.no_prefill and rank == 0:
+        peak_tf, peak_src = measured_peak_bf16_tflops()
+        cases = [("q512_prefill", [512], [512]),
+                 ("prefill_4x4096", [4096] * 4, [4096] * 4),
+                 ("extend_8x(8192+512)", [8704] * 8, [512] * 8)]
+        pf = {}
+        cfgp = W.Config(90, "prefill", 64, 8, "bf16")
+        wanted = [c.strip() for c in args.prefill_cases.split(",") if c.strip()]
+        for name, lens, qn in cases:
+            if name not in wanted:
+                continue
+            wp = W.make_workload(cfgp, lengths=lens, seed=9000)
+            qp, cup = W.make_extend_query(wp, qn, seed=9001)
+            qd, kd, vd = qp.to(dev), wp.k_cache.to(dev), wp.v_cache.to(dev)
+            btd, sld, cud = wp.block_table.to(dev), wp.seq_lens.to(dev), cup.to(dev)
+            od = torch.empty_like(qd)
+            ld = torch.empty(qd.shape[:2], dtype=torch.float32, device=dev)
+            errd = torch.zeros(1, dtype=torch.int32, device=dev)
+
+            def ext():
+                hpc.hpc_extend_attn(qd, kd, vd, btd, sld, cud, od, ld, device_error=errd,
+                                    stream=stream)
+
+            for _ in range(3):
+                flush_l2()
+                ext()
+            es = [[mk(), mk()] for _ in range(max(5, min(args.steps, 20)))]
+            for a, b_ in es:
+                flush_l2()
+                a.record(stream)
+                ext()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            if int(errd.item()) != 0:
+                raise RuntimeError(f"prefill case {name}: device check bits {int(errd.item())}")
+            us = statistics.mean(a.elapsed_time(b_) for a, b_ in es) * 1e3
+            fl = extend_flops(lens, qn, 64)
+            tf = fl / (us * 1e-6) / 1e12
+            pf[name] = {"us": round(us, 2), "flops": fl, "tflops": round(tf, 1),
+                        "frac_of_bf16_peak": round(tf / peak_tf, 4),
+                        "new_tokens": sum(qn), "kv_tokens": sum(lens)}
+            line["gpu_launches"] += len(es)
+            del qd, kd, vd, od, ld
+        pf["peak_tflops"] = peak_tf
+        pf["peak_source"] = peak_src
+        pf["note"] = ("hpc_extend_attn, 64 q / 8 kv heads, d128, bf16 cache; useful causal "
+                      "FLOPs (4*128*H_q per visible key and query row) / CUDA-event time, "
+                      "L2 flushed between launches")
+        line["prefill"] = pf
 
     # ---- context: a plain device-to-device copy on this GPU (read + write bytes)
     if not args.no_copy_probe:

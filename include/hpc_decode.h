@@ -379,6 +379,18 @@ hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
                            hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
                            int32_t* device_error, void* stream);
 
+/* hpc_extend_attn_ex -- hpc_extend_attn with the CTA shape chosen by the
+ * caller: tiles_per_cta = 1 (one 128-row query tile of 16 tokens x 8 heads
+ * per CTA) or 2 (two tiles, 32 tokens, sharing every K / V tile; the
+ * choice for batches that fill the GPU), or 0 for the automatic choice of
+ * hpc_extend_attn (2 when ceil(total_q / 32) * H_kv >= 2 * SMs). Results
+ * are identical either way. Other values give HPC_ERR_INVALID_ARG. */
+hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
+                              const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                              const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
+                              hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
+                              int32_t tiles_per_cta, int32_t* device_error, void* stream);
+
 /* hpc_device_sm_count -- streaming multiprocessors of the current device. */
 hpc_status hpc_device_sm_count(int32_t* num_sms);
 

@@ -106,6 +106,7 @@ def load_library():
             "hpc_rope_norm_kv_write": [T, T, T, T, T, T, T, ctypes.c_float, ctypes.c_float,
                                        T, T, T, T, P, P],
             "hpc_extend_attn": [T, T, T, T, T, T, T, T, ctypes.c_float, P, P],
+            "hpc_extend_attn_ex": [T, T, T, T, T, T, T, T, ctypes.c_float, i32, P, P],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -336,21 +337,23 @@ def hpc_rope_norm_kv_write(q_in, k_in, v_in, seq_lens, block_table, q_norm_weigh
 
 
 def hpc_extend_attn(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse=None,
-                    softmax_scale: Optional[float] = None, device_error=None, stream=None):
+                    softmax_scale: Optional[float] = None, device_error=None, stream=None,
+                    tiles_per_cta: int = 0):
     """Prefill / extend attention on the tensor cores: q and out are bf16
     [total_q][H_q][128] with the new tokens of sequence b in rows
     cu_q_lens[b] .. cu_q_lens[b+1]-1 (the last positions of its cache);
     lse f32 [total_q][H_q] or None; device_error an int32 CUDA tensor
-    receiving HPC_DEVCHK_* bits, or None."""
+    receiving HPC_DEVCHK_* bits, or None; tiles_per_cta 0 (automatic), 1 or 2
+    query tiles of 128 rows per CTA."""
     lib = load_library()
     tq, tk, tv = make_tensor(q), make_tensor(k_cache), make_tensor(v_cache)
     tb, ts, tc = make_tensor(block_table), make_tensor(seq_lens), make_tensor(cu_q_lens)
     to, tl = make_tensor(out), make_tensor(lse)
     ref = lambda d: ctypes.byref(d) if d is not None else None
     err = ctypes.c_void_p(device_error.data_ptr()) if device_error is not None else None
-    _check(lib.hpc_extend_attn(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), ref(tc), ref(to),
-                               ref(tl), ctypes.c_float(softmax_scale or -1.0), err,
-                               _stream_ptr(stream)))
+    _check(lib.hpc_extend_attn_ex(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), ref(tc),
+                                  ref(to), ref(tl), ctypes.c_float(softmax_scale or -1.0),
+                                  int(tiles_per_cta), err, _stream_ptr(stream)))
 
 
 def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int, out,

@@ -853,12 +853,15 @@ hpc_status make_q_map(const hpc_tensor* q, CUtensorMap* map) {
 }  // namespace
 }  // namespace hpc
 
-extern "C" hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
-                                      const hpc_tensor* v_cache, const hpc_tensor* block_table,
-                                      const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
-                                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
-                                      int32_t* device_error, void* stream) {
+extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                         const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                         const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
+                                         hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
+                                         int32_t tiles_per_cta, int32_t* device_error,
+                                         void* stream) {
   using namespace hpc;
+  if (tiles_per_cta < 0 || tiles_per_cta > 2)
+    return fail(HPC_ERR_INVALID_ARG, "tiles_per_cta must be 0 (automatic), 1 or 2");
   hpc_status st;
   if ((st = check_tensor(q, "q", 3)) != HPC_OK) return st;
   if ((st = check_tensor(k_cache, "k_cache", 4)) != HPC_OK) return st;
@@ -922,10 +925,19 @@ extern "C" hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_c
   if (NB == 0) return fail(HPC_ERR_INVALID_ARG, "k_cache has no blocks");
   if (B > INT32_MAX || total_q > INT32_MAX || NB > INT32_MAX || block_table->shape[1] > INT32_MAX)
     return fail(HPC_ERR_INVALID_ARG, "sizes exceed int32");
-  // 16-token tiles: sum_b ceil(n_b / 16) <= total_q / 16 + B
-  const int64_t tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + B;
+  if (tiles_per_cta == 0) {
+    // two 128-row query tiles per CTA when the batch fills the GPU twice over
+    int dev = 0, sms = 0;
+    HPC_CUDA_TRY(cudaGetDevice(&dev));
+    HPC_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const int64_t pairs = (total_q + 2 * kExtendTileTokens - 1) / (2 * kExtendTileTokens);
+    tiles_per_cta = pairs * Hkv >= 2LL * sms ? 2 : 1;
+  }
+  // CTA tiles of T = 16 * tiles_per_cta tokens: sum_b ceil(n_b / T) <= total_q / T + B
+  const int64_t tt = (int64_t)kExtendTileTokens * tiles_per_cta;
+  const int64_t tiles = (total_q + tt - 1) / tt + B;
   if (tiles > 65535)
-    return fail(HPC_ERR_UNSUPPORTED, "too many 16-token tiles in one call (split the batch)");
+    return fail(HPC_ERR_UNSUPPORTED, "too many query tiles in one call (split the batch)");
   CUtensorMap tq, tk, tv;
   if ((st = make_q_map(q, &tq)) != HPC_OK) return st;
   if ((st = make_kv_map(k_cache, false, swap, &tk)) != HPC_OK) return st;
@@ -952,8 +964,17 @@ extern "C" hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_c
   p.score_scale_log2 = scale * 1.4426950408889634f;
   p.err = device_error;
   p.timeout_ns = wait_limit_ns();
-  cudaError_t e = launch_extend(p, tq, tk, tv, (int)tiles, (cudaStream_t)stream);
+  cudaError_t e = launch_extend(p, tq, tk, tv, (int)tiles, tiles_per_cta, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(HPC_ERR_CUDA, std::string("extend launch: ") + cudaGetErrorString(e));
   return HPC_OK;
+}
+
+extern "C" hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                      const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                      const hpc_tensor* seq_lens, const hpc_tensor* cu_q_lens,
+                                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale,
+                                      int32_t* device_error, void* stream) {
+  return hpc_extend_attn_ex(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse,
+                            softmax_scale, 0, device_error, stream);
 }

@@ -43,27 +43,34 @@ namespace {
 
 using namespace tc05;
 
-constexpr int kRows = 128;
-constexpr int kGroupRows = 8;  // query heads per KV head
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kRows = 128;          // query rows of one MMA tile (16 tokens x 8 heads)
+constexpr int kGroupRows = 8;      // query heads per KV head
 constexpr uint32_t kQBytes = kRows * 128 * 2;         // 32 KB: two 16 KB column halves
 constexpr uint32_t kKVTileBytes = 64 * 128 * 2;       // 16 KB: two 8 KB column halves
 constexpr uint32_t kStageBytes = 2 * kKVTileBytes;    // K + V
-constexpr uint32_t kPBytes = kRows * 64 * 2;          // 16 KB: 128 rows x 64 tokens
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kQBytes;
-constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
-// barriers: q_full, kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2], pv_done[2], drain
-constexpr int kNumBars = 1 + 2 * kStages + 8 + 1;
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
-constexpr uint32_t kTmemCols = 256;  // S0 | S1 | O
-constexpr uint32_t kColS = 0, kColO = 128;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// QT query tiles of 128 rows per CTA (QT = 1 or 2). Warps 0 .. 4*QT-1 are
+// the softmax warpgroups (warpgroup g owns tile g: rows = TMEM lanes of its
+// own S and O columns), then one TMA producer warp and one MMA warp.
+template <int QT>
+struct Layout {
+  static constexpr int kProducerWarp = 4 * QT, kMmaWarp = 4 * QT + 1;
+  static constexpr int kThreads = 32 * (4 * QT + 2);
+  static constexpr int kStages = QT == 1 ? 6 : 5;                        // K+V ring depth
+  static constexpr uint32_t kOffQ = 0;                                   // QT x 32 KB
+  static constexpr uint32_t kOffKV = QT * kQBytes;                       // stages x 32 KB
+  static constexpr uint32_t kOffBar = kOffKV + kStages * kStageBytes;
+  // q_full, kv_full[S], kv_empty[S], per tile: s_full, s_free, p_full[2], pv_done[2]; drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 6 * QT + 1;
+  static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align to 1024
+  // tensor memory per query tile: S (64 columns) | P0, P1 (32 each, bf16 pairs) | O (128)
+  static constexpr uint32_t kTmemCols = 256 * QT;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+constexpr uint32_t kColS = 0, kColP = 64, kColO = 128;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -116,10 +123,10 @@ struct TileInfo {
 };
 
 // Warp-cooperative: map tile index y (heaviest first) to (sequence, tile).
-// Every sequence contributes ceil(n_b / 16) tiles; tiles are numbered in
+// Every sequence contributes ceil(n_b / tile_tokens) tiles; tiles are numbered in
 // sequence order and y counts from the last one, so the CTAs launched first
 // take the tiles that see the most keys.
-__device__ TileInfo find_tile(const ExtendParams& p, int y, int lane) {
+__device__ TileInfo find_tile(const ExtendParams& p, int y, int lane, int tile_tokens) {
   TileInfo ti;
   ti.valid = 0;
   const int B = p.num_seqs;
@@ -129,7 +136,7 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane) {
     int nt = 0;
     if (b < B) {
       const int n = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
-      nt = n > 0 ? (n + kExtendTileTokens - 1) / kExtendTileTokens : 0;
+      nt = n > 0 ? (n + tile_tokens - 1) / tile_tokens : 0;
     }
     total += warp_sum_i(nt);
   }
@@ -141,7 +148,7 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane) {
     int nt = 0;
     if (b < B) {
       const int n = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
-      nt = n > 0 ? (n + kExtendTileTokens - 1) / kExtendTileTokens : 0;
+      nt = n > 0 ? (n + tile_tokens - 1) / tile_tokens : 0;
     }
     int incl = nt;
 #pragma unroll
@@ -156,7 +163,7 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane) {
       const int incl_f = __shfl_sync(0xffffffffu, incl, f);
       const int nt_f = __shfl_sync(0xffffffffu, nt, f);
       ti.b = c + f;
-      ti.t0 = (gx - (base + incl_f - nt_f)) * kExtendTileTokens;
+      ti.t0 = (gx - (base + incl_f - nt_f)) * tile_tokens;
       ti.valid = 1;
       break;
     }
@@ -171,44 +178,54 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane) {
     ti.valid = 0;
     return ti;
   }
-  // keys seen by the tile's last token (padding rows past n clamp to L)
-  int kv_len = ti.L - ti.n + ti.t0 + kExtendTileTokens;
-  if (kv_len > ti.L) kv_len = ti.L;
-  ti.n_kv = (kv_len + 63) / 64;
+  ti.n_kv = 0;  // per query tile, see tile_kv()
   return ti;
+}
+
+// KV tiles read by query tile g of a CTA (16 tokens from t0 + 16 g): the keys
+// its last row sees (rows past n clamp to L); 0 when the tile has no row.
+__device__ __forceinline__ int tile_kv(int L, int n, int t0g) {
+  if (t0g >= n) return 0;
+  int kv_len = L - n + t0g + kExtendTileTokens;
+  if (kv_len > L) kv_len = L;
+  return (kv_len + 63) / 64;
 }
 
 }  // namespace
 
 namespace {
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int QT>
+__global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
     extend_kernel(const __grid_constant__ ExtendParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+  using Lt = Layout<QT>;
+  constexpr int S = Lt::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-B alignment
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + kOffQ, sKV = base + kOffKV, sP = base + kOffP;
-  const uint32_t bars = base + kOffBar;
+  const uint32_t sQ = base + Lt::kOffQ, sKV = base + Lt::kOffKV;
+  const uint32_t bars = base + Lt::kOffBar;
   const uint32_t bar_q = bars;
   auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bars + 8u * (1 + kStages + s); };
-  auto s_full = [&](int i) { return bars + 8u * (1 + 2 * kStages + i); };
-  auto s_free = [&](int i) { return bars + 8u * (3 + 2 * kStages + i); };
-  auto p_full = [&](int i) { return bars + 8u * (5 + 2 * kStages + i); };
-  auto pv_done = [&](int i) { return bars + 8u * (7 + 2 * kStages + i); };
-  const uint32_t bar_drain = bars + 8u * (9 + 2 * kStages);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int* s_info = reinterpret_cast<int*>(smem + kOffMisc + 8);
+  auto kv_empty = [&](int s) { return bars + 8u * (1 + S + s); };
+  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 6 * g + k); };
+  auto s_full = [&](int g) { return gbar(g, 0); };
+  auto s_free = [&](int g) { return gbar(g, 1); };
+  auto p_full = [&](int g, int i) { return gbar(g, 2 + i); };
+  auto pv_done = [&](int g, int i) { return gbar(g, 4 + i); };
+  const uint32_t bar_drain = bars + 8u * (1 + 2 * S + 6 * QT);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lt::kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Lt::kOffMisc + 4);
+  int* s_info = reinterpret_cast<int*>(smem + Lt::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x;
   const unsigned long long lim_ns = p.timeout_ns;
 
   if (warp == 0) {
-    const TileInfo ti = find_tile(p, blockIdx.y, lane);
+    const TileInfo ti = find_tile(p, blockIdx.y, lane, kExtendTileTokens * QT);
     if (lane == 0) {
       s_info[0] = ti.valid;
       s_info[1] = ti.b;
@@ -216,20 +233,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_info[3] = ti.n;
       s_info[4] = ti.L;
       s_info[5] = ti.q0;
-      s_info[6] = ti.valid ? ti.n_kv : 0;
     }
-  } else if (warp == kProducerWarp) {
+  } else if (warp == Lt::kProducerWarp) {
     if (lane == 0) {
       mbar_init(bar_q, 1);
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < S; ++s) {
         mbar_init(kv_full(s), 1);
         mbar_init(kv_empty(s), 1);
       }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(s_full(i), 1);
-        mbar_init(s_free(i), kRows);
-        mbar_init(p_full(i), kRows);
-        mbar_init(pv_done(i), 1);
+      for (int g = 0; g < QT; ++g) {
+        mbar_init(s_full(g), 1);
+        mbar_init(s_free(g), kRows);
+        for (int i = 0; i < 2; ++i) {
+          mbar_init(p_full(g, i), kRows);
+          mbar_init(pv_done(g, i), 1);
+        }
       }
       mbar_init(bar_drain, 1);
       *s_abort = 0;
@@ -238,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_map(&tmk);
       prefetch_map(&tmv);
     }
-  } else if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+  } else if (warp == Lt::kMmaWarp) {
+    tmem_alloc(smem_u32(s_tmem), Lt::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -247,18 +265,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   const int valid = s_info[0], b = s_info[1], t0 = s_info[2], n = s_info[3], L = s_info[4],
-            q0 = s_info[5], n_kv = s_info[6];
+            q0 = s_info[5];
+  int nkv[QT];
+  int n_kv = 0;
+#pragma unroll
+  for (int g = 0; g < QT; ++g) {
+    nkv[g] = valid ? tile_kv(L, n, t0 + kExtendTileTokens * g) : 0;
+    n_kv = nkv[g] > n_kv ? nkv[g] : n_kv;
+  }
   const uint32_t tmem = *s_tmem;
   int32_t* err = p.err;
 
-  if (warp == kProducerWarp) {
+  if (warp == Lt::kProducerWarp) {
     // ------------------------------------------------------------ producer
     int issued = 0;  // K/V tiles whose copies were issued (in order)
-    if (valid && n_kv > 0) {
+    if (n_kv > 0) {
       if (lane == 0) {
-        mbar_expect_tx(bar_q, kQBytes);
-        tma_load_3d(sQ, &tmq, bar_q, 0, kGroupRows * h, q0 + t0);
-        tma_load_3d(sQ + kQBytes / 2, &tmq, bar_q, 64, kGroupRows * h, q0 + t0);
+        mbar_expect_tx(bar_q, QT * kQBytes);
+#pragma unroll
+        for (int g = 0; g < QT; ++g) {
+          const int row = q0 + t0 + kExtendTileTokens * g;
+          tma_load_3d(sQ + g * kQBytes, &tmq, bar_q, 0, kGroupRows * h, row);
+          tma_load_3d(sQ + g * kQBytes + kQBytes / 2, &tmq, bar_q, 64, kGroupRows * h, row);
+        }
       }
       const int c1 = p.kv_swap ? h : 0, c2 = p.kv_swap ? 0 : h;
       int stop = 0;
@@ -277,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < cnt; ++u) {
           const int bk = __shfl_sync(0xffffffffu, blk, u);
           if (lane == 0) {
-            const int j = j0 + u, slot = j % kStages, round = j / kStages;
-            bool ok = round == 0 ||
-                      wait_bar(kv_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
+            const int j = j0 + u, slot = j % S, round = j / S;
+            const bool ok =
+                round == 0 || wait_bar(kv_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
             if (ok) {
               const uint32_t fb = kv_full(slot);
               const uint32_t dk = sKV + slot * kStageBytes, dv = dk + kKVTileBytes;
@@ -298,108 +327,161 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    named_bar_sync(1, kThreads);
+    named_bar_sync(1, Lt::kThreads);
     // drain: the last copy issued into each slot has landed
     if (lane == 0) {
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int rounds = (issued - s + kStages - 1) / kStages;
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int rounds = (issued - s + S - 1) / S;
         wait_bar(kv_full(s), (rounds - 1) & 1, s_abort, err, lim_ns, false);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == Lt::kMmaWarp) {
     // ----------------------------------------------------------- MMA issue
+    // The whole warp runs the schedule (waits, descriptor arithmetic) so its
+    // values stay warp-uniform; one elected lane issues the MMAs and commits.
+    // Descriptors are formed once; per K step only immediates are added to
+    // the start-address field (bits 0..13, bytes >> 4).
+    const bool leader = elect_one() != 0;
     bool issued_any = false;
-    if (valid && n_kv > 0 && lane == 0) {
+    if (n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kRows, 64, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kRows, 128, false, true);
-      auto issue_pv = [&](int i) -> bool {
-        if (!wait_bar(p_full(i & 1), (i >> 1) & 1, s_abort, err, lim_ns)) return false;
+      const uint64_t qd0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sKV, 16, 1024);
+      // V: MN-major; 64-column halves 8 KB apart, 8-token row groups 1 KB apart
+      const uint64_t vd0 = smem_desc_sw128(sKV + kKVTileBytes, kKVTileBytes / 2, 1024);
+      // O_g += P_g V_i, P from tensor memory (16 keys = 8 columns per step)
+      auto issue_pv = [&](int g, int i) -> bool {
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(p_full(g, i & 1), (i >> 1) & 1, s_abort, err, lim_ns)))
+          return false;
         tc_fence_after();
-        const uint32_t vb = sKV + (i % kStages) * kStageBytes + kKVTileBytes;
-        const uint32_t pb = sP + (i & 1) * kPBytes;
+        const uint64_t vd = vd0 + (uint64_t)((i % S) * (kStageBytes >> 4));
+        const uint32_t pa = tmem + 256u * g + kColP + 32u * (uint32_t)(i & 1);
+        const uint32_t od = tmem + 256u * g + kColO;
+        if (leader) {
+          mma_f16_ts(od, pa, vd, kIdPV, i > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          // P: K-major, 16 tokens = 32 bytes along the swizzled row
-          const uint64_t a = smem_desc_sw128(pb + kk * 32, 16, 1024);
-          // V: MN-major; 64-column halves 8 KB apart, 8-token row groups 1 KB apart
-          const uint64_t bd = smem_desc_sw128(vb + kk * 2048, kKVTileBytes / 2, 1024);
-          mma_f16_ss(tmem + kColO, a, bd, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 1; kk < 4; ++kk)
+            mma_f16_ts(od, pa + 8 * kk, vd + kk * (2048 >> 4), kIdPV, 1u);
+          mma_commit(pv_done(g, i & 1));
         }
-        mma_commit(pv_done(i & 1));
-        mma_commit(kv_empty(i % kStages));
+        __syncwarp();
         return true;
       };
-      bool ok = wait_bar(bar_q, 0, s_abort, err, lim_ns);
+      bool ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int slot = j % kStages;
-        ok = wait_bar(kv_full(slot), (j / kStages) & 1, s_abort, err, lim_ns);
-        if (ok && j >= 2) ok = wait_bar(s_free(j & 1), ((j - 2) >> 1) & 1, s_abort, err, lim_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = sKV + slot * kStageBytes;
-        const uint32_t dS = tmem + kColS + (uint32_t)(j & 1) * 64;
+        const int slot = j % S;
+        ok = __all_sync(0xffffffffu, wait_bar(kv_full(slot), (j / S) & 1, s_abort, err, lim_ns));
+        const uint64_t kd = kd0 + (uint64_t)(slot * (kStageBytes >> 4));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // Q and K: K-major; 64-column halves (16 KB / 8 KB apart), 16 columns = 32 bytes
-          const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * (kKVTileBytes / 2) + (kk & 3) * 32, 16, 1024);
-          mma_f16_ss(dS, a, bd, kIdS, kk > 0 ? 1u : 0u);
+        for (int g = 0; g < QT; ++g) {
+          if (!ok || j >= nkv[g]) continue;
+          // S_g is single-buffered: its softmax warps have copied S_g(j-1) out
+          if (j >= 1)
+            ok = __all_sync(0xffffffffu, wait_bar(s_free(g), (j - 1) & 1, s_abort, err, lim_ns));
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t qd = qd0 + (uint64_t)(g * (kQBytes >> 4));
+          const uint32_t dS = tmem + 256u * g + kColS;
+          if (leader) {
+            // Q and K: K-major; 64-column halves (16 KB / 8 KB apart), 16 columns = 32 bytes
+            mma_f16_ss(dS, qd, kd, kIdS, 0u);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk)
+              mma_f16_ss(dS, qd + (kk >> 2) * ((kQBytes / 2) >> 4) + (kk & 3) * 2,
+                         kd + (kk >> 2) * ((kKVTileBytes / 2) >> 4) + (kk & 3) * 2, kIdS, 1u);
+            mma_commit(s_full(g));
+          }
+          __syncwarp();
+          issued_any = true;
         }
-        issued_any = true;
-        mma_commit(s_full(j & 1));
-        if (j >= 1) ok = issue_pv(j - 1);
+        if (ok && j >= 1) {
+#pragma unroll
+          for (int g = 0; g < QT; ++g)
+            if (ok && j - 1 < nkv[g]) ok = issue_pv(g, j - 1);
+          if (ok && leader) mma_commit(kv_empty((j - 1) % S));
+          __syncwarp();
+        }
       }
-      if (ok) issue_pv(n_kv - 1);
+#pragma unroll
+      for (int g = 0; g < QT; ++g)
+        if (ok && n_kv - 1 < nkv[g]) ok = issue_pv(g, n_kv - 1);
     }
-    named_bar_sync(1, kThreads);
-    if (lane == 0 && issued_any) {
-      mma_commit(bar_drain);  // every MMA of this CTA has completed
+    named_bar_sync(1, Lt::kThreads);
+    if (leader && issued_any) {
+      mma_commit(bar_drain);  // every MMA this lane issued has completed
       wait_bar(bar_drain, 0, s_abort, err, lim_ns, false);
     }
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  } else if (warp < 4) {
-    // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;  // query row = TMEM lane
-    const int g = r & 7, tok = t0 + (r >> 3);
+    tmem_dealloc(tmem, Lt::kTmemCols);
+  } else {
+    // ------------------------------------------------ softmax warpgroup g
+    const int g = warp >> 2;
+    const int r = threadIdx.x - kRows * g;  // query row = TMEM lane
+    const int tok = t0 + kExtendTileTokens * g + (r >> 3), head = kGroupRows * h + (r & 7);
     const bool row_ok = valid && tok < n;
     int lim = L - n + 1 + tok;  // keys visible to this row: positions < lim
     if (lim > L) lim = L;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const int nk = g == 0 ? nkv[0] : nkv[QT - 1];
+    const uint32_t trow = tmem + 256u * g + ((uint32_t)((warp & 3) * 32) << 16);
     const float sc = p.score_scale_log2;
     float m = -INFINITY, l = 0.f;
-    bool ok = valid && n_kv > 0;
-    for (int j = 0; ok && j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bar(s_full(j & 1), (j >> 1) & 1, s_abort, err, lim_ns));
+    bool ok = nk > 0;
+    for (int j = 0; ok && j < nk; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bar(s_full(g), j & 1, s_abort, err, lim_ns));
       if (!ok) break;
       tc_fence_after();
       float s[64];
-      tmem_ld32(trow + kColS + (uint32_t)(j & 1) * 64, *reinterpret_cast<float(*)[32]>(&s[0]));
-      tmem_ld32(trow + kColS + (uint32_t)(j & 1) * 64 + 32,
-                *reinterpret_cast<float(*)[32]>(&s[32]));
+      tmem_ld32(trow + kColS, *reinterpret_cast<float(*)[32]>(&s[0]));
+      tmem_ld32(trow + kColS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(s_free(j & 1));
+      mbar_arrive(s_free(g));
       const int kv0 = j * 64;
       if (kv0 + 64 > lim) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (kv0 + c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row maximum by a tree (eight independent chains)
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 64; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m, mx * sc);
-      const bool need = m_new > m + kRescaleThreshold;
-      if (j == 0) {
-        m = m_new;
-      } else if (__any_sync(0xffffffffu, need)) {
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, s_abort, err, lim_ns));
+      // move the row maximum only when it grew by more than the threshold
+      const bool need = j > 0 && m_new > m + kRescaleThreshold;
+      const float m_use = (j == 0 || need) ? m_new : m;
+      const float alpha = need ? ex2(m - m_new) : 1.f;
+      uint32_t pk[32];
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = -m_use;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(s[2 * c], sc, nm));
+        const float p1 = ex2(fmaf(s[2 * c + 1], sc, nm));
+        rs4[c & 3] += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c + 1
+      }
+      l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      m = m_use;
+      if (j >= 2) {
+        // the PV that read this P buffer (tile j - 2) is done
+        ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, j & 1), ((j - 2) >> 1) & 1, s_abort,
+                                              err, lim_ns));
+        if (!ok) break;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // O is stable once the PV of tile j - 1 is done
+        ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, (j - 1) & 1), ((j - 1) >> 1) & 1,
+                                              s_abort, err, lim_ns));
         if (!ok) break;
         tc_fence_after();
-        const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float o[32];
@@ -409,51 +491,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
           tmem_st32(trow + kColO + q * 32, o);
         }
-        tmem_wait_st();
-        if (need) {
-          l *= alpha;
-          m = m_new;
-        }
+      } else if (j >= 2) {
+        tc_fence_after();
       }
-      uint32_t pk[32];
-      float rs = 0.f;
-      const float nm = -m;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sc, nm));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sc, nm));
-        rs += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
-      }
-      l += rs;
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(pv_done(j & 1), ((j - 2) >> 1) & 1, s_abort, err, lim_ns));
-        if (!ok) break;
-      }
-      // row r of the K-major 128-byte-swizzled P tile: 16-byte chunk c -> c ^ (r % 8)
-      const uint32_t prow = sP + (uint32_t)(j & 1) * kPBytes + (uint32_t)r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         prow + ((uint32_t)(ch ^ (r & 7)) << 4)),
-                     "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
-                     "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
-      fence_async_shared();
+      // P (bf16 pairs) into this tile's tensor-memory buffer: row = lane
+      tmem_st32(trow + kColP + 32u * (uint32_t)(j & 1), pk);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full(j & 1));
+      mbar_arrive(p_full(g, j & 1));
     }
     if (ok) {
-      ok = __all_sync(0xffffffffu, wait_bar(pv_done((n_kv - 1) & 1), ((n_kv - 1) >> 1) & 1,
+      ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, (nk - 1) & 1), ((nk - 1) >> 1) & 1,
                                             s_abort, err, lim_ns));
     }
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow =
-          p.out + (int64_t)(q0 + tok) * p.o_st + (int64_t)(kGroupRows * h + g) * p.o_sh;
+      __nv_bfloat16* orow = p.out + (int64_t)(q0 + tok) * p.o_st + (int64_t)head * p.o_sh;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float o[32];
@@ -472,28 +526,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_ok && p.lse)
-        p.lse[(int64_t)(q0 + tok) * p.l_st + (int64_t)(kGroupRows * h + g) * p.l_sh] =
+        p.lse[(int64_t)(q0 + tok) * p.l_st + (int64_t)head * p.l_sh] =
             l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
     tc_fence_before();
-    named_bar_sync(1, kThreads);
+    named_bar_sync(1, Lt::kThreads);
   }
+}
+
+template <int QT>
+cudaError_t launch_qt(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const CUtensorMap& tv, int tiles, cudaStream_t stream) {
+  using Lt = Layout<QT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(extend_kernel<QT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lt::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  extend_kernel<QT><<<dim3(p.num_kv_heads, tiles), Lt::kThreads, Lt::kSmemBytes, stream>>>(
+      p, tq, tk, tv);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_extend(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int tiles, cudaStream_t stream) {
+                          const CUtensorMap& tv, int tiles, int tiles_per_cta,
+                          cudaStream_t stream) {
   if (tiles <= 0 || p.num_kv_heads <= 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  extend_kernel<<<dim3(p.num_kv_heads, tiles), kThreads, kSmemBytes, stream>>>(p, tq, tk, tv);
-  return cudaGetLastError();
+  if (tiles_per_cta == 2) return launch_qt<2>(p, tq, tk, tv, tiles, stream);
+  return launch_qt<1>(p, tq, tk, tv, tiles, stream);
 }
 
 }  // namespace hpc

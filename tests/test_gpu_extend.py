@@ -26,7 +26,7 @@ def _cfg(hq, hkv):
     return W.Config(95, "extend", hq, hkv, "bf16")
 
 
-def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err=0):
+def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err=0, tpc=0):
     dev = "cuda"
     qd = q.to(dev)
     out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
@@ -35,7 +35,8 @@ def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err
     hpc.hpc_extend_attn(qd, w.k_cache.to(dev) if k is None else k,
                         w.v_cache.to(dev) if v is None else v,
                         w.block_table.to(dev) if bt is None else bt, w.seq_lens.to(dev),
-                        cu.to(dev), out, lse, softmax_scale=softmax_scale, device_error=err)
+                        cu.to(dev), out, lse, softmax_scale=softmax_scale, device_error=err,
+                        tiles_per_cta=tpc)
     torch.cuda.synchronize()
     assert int(err.item()) == expect_err, f"device check bits {int(err.item())}"
     return out, lse
@@ -63,10 +64,15 @@ CASES = [
 def test_matches_oracle(hq, hkv, lens, qn):
     w = W.make_workload(_cfg(hq, hkv), lengths=lens, seed=40 + len(lens))
     q, cu = W.make_extend_query(w, qn, seed=41)
-    out, lse = run_extend(w, q, cu)
     ref_out, ref_lse = _oracle(w, q, cu)
-    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
-                  label=f"extend {lens} {qn}")
+    outs = []
+    for tpc in (1, 2):  # one or two 128-row query tiles per CTA
+        out, lse = run_extend(w, q, cu, tpc=tpc)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      label=f"extend {lens} {qn} tiles/CTA {tpc}")
+        outs.append((out, lse))
+    # the CTA shape changes which rows share a CTA, not any row's arithmetic
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def test_sharp_softmax_and_explicit_scale():
@@ -74,11 +80,11 @@ def test_sharp_softmax_and_explicit_scale():
     # O rescale path runs; a second scale checks the scale argument
     w = W.make_workload(_cfg(64, 8), lengths=[700, 129], seed=42)
     q, cu = W.make_extend_query(w, [300, 129], seed=43, q_scale=8.0)
-    for scale in (None, 0.05):
-        out, lse = run_extend(w, q, cu, softmax_scale=scale)
+    for scale, tpc in ((None, 1), (None, 2), (0.05, 2)):
+        out, lse = run_extend(w, q, cu, softmax_scale=scale, tpc=tpc)
         ref_out, ref_lse = _oracle(w, q, cu, softmax_scale=scale)
         assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
-                      label=f"sharp scale={scale}")
+                      label=f"sharp scale={scale} tiles/CTA {tpc}")
 
 
 def test_block_permutation_and_layout_invariance():
@@ -109,8 +115,10 @@ def test_large_prefill_sampled_rows():
     lens = [4096] * 4
     w = W.make_workload(_cfg(64, 8), lengths=lens, seed=47)
     q, cu = W.make_extend_query(w, lens, seed=48)
-    out, lse = run_extend(w, q, cu)
+    out, lse = run_extend(w, q, cu)   # automatic: two query tiles per CTA at this size
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    out1, lse1 = run_extend(w, q, cu, tpc=1)
+    assert torch.equal(out, out1) and torch.equal(lse, lse1)
     g = torch.Generator().manual_seed(49)
     rows = sorted(set([0, 15, 16, 4095, 4096, 8191, 12287, 16383] +
                       torch.randint(0, 16384, (56,), generator=g).tolist()))
@@ -141,6 +149,9 @@ def test_argument_and_device_checks():
     with pytest.raises(hpc.HpcError) as e:
         hpc.hpc_extend_attn(args[0], k8, k8, *args[3:])
     assert e.value.status == hpc.HPC_ERR_UNSUPPORTED
+    with pytest.raises(hpc.HpcError) as e:
+        hpc.hpc_extend_attn(*args, tiles_per_cta=3)
+    assert e.value.status == hpc.HPC_ERR_INVALID_ARG
     # cu_q_lens of the wrong length
     with pytest.raises(hpc.HpcError) as e:
         hpc.hpc_extend_attn(*args[:5], cu[:2].to(dev), out)
