@@ -53,17 +53,18 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // QT query tiles of 128 rows per CTA (QT = 1 or 2). Warps 0 .. 4*QT-1 are
 // the softmax warpgroups (warpgroup g owns tile g: rows = TMEM lanes of its
-// own S and O columns), then one TMA producer warp and one MMA warp.
+// own S and O columns), then one TMA producer warp and one MMA warp per query
+// tile, so the two tiles' S -> softmax -> P*V chains never wait on each other.
 template <int QT>
 struct Layout {
-  static constexpr int kProducerWarp = 4 * QT, kMmaWarp = 4 * QT + 1;
-  static constexpr int kThreads = 32 * (4 * QT + 2);
+  static constexpr int kProducerWarp = 4 * QT, kMmaWarp0 = 4 * QT + 1;
+  static constexpr int kThreads = 32 * (5 * QT + 1);
   static constexpr int kStages = QT == 1 ? 6 : 5;                        // K+V ring depth
   static constexpr uint32_t kOffQ = 0;                                   // QT x 32 KB
   static constexpr uint32_t kOffKV = QT * kQBytes;                       // stages x 32 KB
   static constexpr uint32_t kOffBar = kOffKV + kStages * kStageBytes;
-  // q_full, kv_full[S], kv_empty[S], per tile: s_full, s_free, p_full[2], pv_done[2]; drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 6 * QT + 1;
+  // q_full, kv_full[S], kv_empty[S], per tile: s_full, s_free, p_full[2], pv_done[2], drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 7 * QT;
   static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align to 1024
   // tensor memory per query tile: S (64 columns) | P0, P1 (32 each, bf16 pairs) | O (128)
@@ -210,12 +211,12 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
   const uint32_t bar_q = bars;
   auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
   auto kv_empty = [&](int s) { return bars + 8u * (1 + S + s); };
-  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 6 * g + k); };
+  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 7 * g + k); };
   auto s_full = [&](int g) { return gbar(g, 0); };
   auto s_free = [&](int g) { return gbar(g, 1); };
   auto p_full = [&](int g, int i) { return gbar(g, 2 + i); };
   auto pv_done = [&](int g, int i) { return gbar(g, 4 + i); };
-  const uint32_t bar_drain = bars + 8u * (1 + 2 * S + 6 * QT);
+  auto drain = [&](int g) { return gbar(g, 6); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lt::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Lt::kOffMisc + 4);
   int* s_info = reinterpret_cast<int*>(smem + Lt::kOffMisc + 8);
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
       mbar_init(bar_q, 1);
       for (int s = 0; s < S; ++s) {
         mbar_init(kv_full(s), 1);
-        mbar_init(kv_empty(s), 1);
+        mbar_init(kv_empty(s), QT);  // one arrival per query tile's MMA warp
       }
       for (int g = 0; g < QT; ++g) {
         mbar_init(s_full(g), 1);
@@ -248,15 +249,15 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
           mbar_init(p_full(g, i), kRows);
           mbar_init(pv_done(g, i), 1);
         }
+        mbar_init(drain(g), 1);
       }
-      mbar_init(bar_drain, 1);
       *s_abort = 0;
       fence_barrier_init();
       prefetch_map(&tmq);
       prefetch_map(&tmk);
       prefetch_map(&tmv);
     }
-  } else if (warp == Lt::kMmaWarp) {
+  } else if (warp == Lt::kMmaWarp0) {
     tmem_alloc(smem_u32(s_tmem), Lt::kTmemCols);
     tmem_relinquish();
   }
@@ -335,87 +336,85 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
         wait_bar(kv_full(s), (rounds - 1) & 1, s_abort, err, lim_ns, false);
       }
     }
-  } else if (warp == Lt::kMmaWarp) {
-    // ----------------------------------------------------------- MMA issue
+  } else if (warp >= Lt::kMmaWarp0) {
+    // ---------------------------------------------- MMA issue for tile g
     // The whole warp runs the schedule (waits, descriptor arithmetic) so its
     // values stay warp-uniform; one elected lane issues the MMAs and commits.
     // Descriptors are formed once; per K step only immediates are added to
     // the start-address field (bits 0..13, bytes >> 4).
+    const int g = warp - Lt::kMmaWarp0;
+    const int nkg = g == 0 ? nkv[0] : nkv[QT - 1];
     const bool leader = elect_one() != 0;
     bool issued_any = false;
     if (n_kv > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kRows, 64, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(kRows, 128, false, true);
-      const uint64_t qd0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t qd = smem_desc_sw128(sQ + g * kQBytes, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sKV, 16, 1024);
       // V: MN-major; 64-column halves 8 KB apart, 8-token row groups 1 KB apart
       const uint64_t vd0 = smem_desc_sw128(sKV + kKVTileBytes, kKVTileBytes / 2, 1024);
-      // O_g += P_g V_i, P from tensor memory (16 keys = 8 columns per step)
-      auto issue_pv = [&](int g, int i) -> bool {
+      const uint32_t dS = tmem + 256u * g + kColS, od = tmem + 256u * g + kColO;
+      // O_g += P_g V_i, P from tensor memory (16 keys = 8 columns per step);
+      // the K/V slot of tile i is released once this tile's MMAs on it are done
+      auto issue_pv = [&](int i) -> bool {
         if (!__all_sync(0xffffffffu,
                         wait_bar(p_full(g, i & 1), (i >> 1) & 1, s_abort, err, lim_ns)))
           return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((i % S) * (kStageBytes >> 4));
         const uint32_t pa = tmem + 256u * g + kColP + 32u * (uint32_t)(i & 1);
-        const uint32_t od = tmem + 256u * g + kColO;
         if (leader) {
           mma_f16_ts(od, pa, vd, kIdPV, i > 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 1; kk < 4; ++kk)
             mma_f16_ts(od, pa + 8 * kk, vd + kk * (2048 >> 4), kIdPV, 1u);
           mma_commit(pv_done(g, i & 1));
+          mma_commit(kv_empty(i % S));
         }
         __syncwarp();
         return true;
       };
       bool ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
-      for (int j = 0; ok && j < n_kv; ++j) {
+      for (int j = 0; ok && j < nkg; ++j) {
         const int slot = j % S;
         ok = __all_sync(0xffffffffu, wait_bar(kv_full(slot), (j / S) & 1, s_abort, err, lim_ns));
+        // S_g is single-buffered: the softmax warps have copied S_g(j-1) out
+        if (ok && j >= 1)
+          ok = __all_sync(0xffffffffu, wait_bar(s_free(g), (j - 1) & 1, s_abort, err, lim_ns));
+        if (!ok) break;
+        tc_fence_after();
         const uint64_t kd = kd0 + (uint64_t)(slot * (kStageBytes >> 4));
+        if (leader) {
+          // Q and K: K-major; 64-column halves (16 KB / 8 KB apart), 16 columns = 32 bytes
+          mma_f16_ss(dS, qd, kd, kIdS, 0u);
 #pragma unroll
-        for (int g = 0; g < QT; ++g) {
-          if (!ok || j >= nkv[g]) continue;
-          // S_g is single-buffered: its softmax warps have copied S_g(j-1) out
-          if (j >= 1)
-            ok = __all_sync(0xffffffffu, wait_bar(s_free(g), (j - 1) & 1, s_abort, err, lim_ns));
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t qd = qd0 + (uint64_t)(g * (kQBytes >> 4));
-          const uint32_t dS = tmem + 256u * g + kColS;
-          if (leader) {
-            // Q and K: K-major; 64-column halves (16 KB / 8 KB apart), 16 columns = 32 bytes
-            mma_f16_ss(dS, qd, kd, kIdS, 0u);
-#pragma unroll
-            for (int kk = 1; kk < 8; ++kk)
-              mma_f16_ss(dS, qd + (kk >> 2) * ((kQBytes / 2) >> 4) + (kk & 3) * 2,
-                         kd + (kk >> 2) * ((kKVTileBytes / 2) >> 4) + (kk & 3) * 2, kIdS, 1u);
-            mma_commit(s_full(g));
-          }
-          __syncwarp();
-          issued_any = true;
+          for (int kk = 1; kk < 8; ++kk)
+            mma_f16_ss(dS, qd + (kk >> 2) * ((kQBytes / 2) >> 4) + (kk & 3) * 2,
+                       kd + (kk >> 2) * ((kKVTileBytes / 2) >> 4) + (kk & 3) * 2, kIdS, 1u);
+          mma_commit(s_full(g));
         }
-        if (ok && j >= 1) {
-#pragma unroll
-          for (int g = 0; g < QT; ++g)
-            if (ok && j - 1 < nkv[g]) ok = issue_pv(g, j - 1);
-          if (ok && leader) mma_commit(kv_empty((j - 1) % S));
-          __syncwarp();
-        }
+        __syncwarp();
+        issued_any = true;
+        if (j >= 1) ok = issue_pv(j - 1);
       }
-#pragma unroll
-      for (int g = 0; g < QT; ++g)
-        if (ok && n_kv - 1 < nkv[g]) ok = issue_pv(g, n_kv - 1);
+      if (ok && nkg > 0) ok = issue_pv(nkg - 1);
+      // K/V tiles this query tile does not read still get its arrival, in the
+      // right round: once the tile has landed, the slot's previous round is over
+      for (int j = nkg; ok && j < n_kv; ++j) {
+        ok = __all_sync(0xffffffffu, wait_bar(kv_full(j % S), (j / S) & 1, s_abort, err, lim_ns));
+        if (ok && leader) mbar_arrive(kv_empty(j % S));
+        __syncwarp();
+      }
     }
-    named_bar_sync(1, Lt::kThreads);
     if (leader && issued_any) {
-      mma_commit(bar_drain);  // every MMA this lane issued has completed
-      wait_bar(bar_drain, 0, s_abort, err, lim_ns, false);
+      mma_commit(drain(g));  // every MMA this lane issued has completed
+      wait_bar(drain(g), 0, s_abort, err, lim_ns, false);
     }
     __syncwarp();
+    tc_fence_before();
+    named_bar_sync(1, Lt::kThreads);
     tc_fence_after();
-    tmem_dealloc(tmem, Lt::kTmemCols);
+    if (warp == Lt::kMmaWarp0) tmem_dealloc(tmem, Lt::kTmemCols);
   } else {
     // ------------------------------------------------ softmax warpgroup g
     const int g = warp >> 2;
