@@ -83,6 +83,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Packed pairs of f32 (sm_100+ paired FMA / add): one instruction, two lanes.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -374,14 +398,16 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
         __syncwarp();
         return true;
       };
-      bool ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
-      for (int j = 0; ok && j < nkg; ++j) {
+      // S_g(j) = Q_g K_j^T; S is single-buffered, so S(j) waits until the
+      // softmax warps have copied S(j-1) out (early in their tile j-1)
+      auto issue_s = [&](int j) -> bool {
         const int slot = j % S;
-        ok = __all_sync(0xffffffffu, wait_bar(kv_full(slot), (j / S) & 1, s_abort, err, lim_ns));
-        // S_g is single-buffered: the softmax warps have copied S_g(j-1) out
-        if (ok && j >= 1)
-          ok = __all_sync(0xffffffffu, wait_bar(s_free(g), (j - 1) & 1, s_abort, err, lim_ns));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu,
+                        wait_bar(kv_full(slot), (j / S) & 1, s_abort, err, lim_ns)))
+          return false;
+        if (j >= 1 && !__all_sync(0xffffffffu,
+                                  wait_bar(s_free(g), (j - 1) & 1, s_abort, err, lim_ns)))
+          return false;
         tc_fence_after();
         const uint64_t kd = kd0 + (uint64_t)(slot * (kStageBytes >> 4));
         if (leader) {
@@ -394,10 +420,19 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
           mma_commit(s_full(g));
         }
         __syncwarp();
+        return true;
+      };
+      // software pipeline: S(j+1) runs on the tensor cores while the softmax
+      // warps work on tile j; P(j) V_j follows once P(j) is written
+      bool ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
+      if (ok && nkg > 0) {
+        ok = issue_s(0);
         issued_any = true;
-        if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok && nkg > 0) ok = issue_pv(nkg - 1);
+      for (int j = 0; ok && j < nkg; ++j) {
+        if (j + 1 < nkg) ok = issue_s(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
       // K/V tiles this query tile does not read still get its arrival, in the
       // right round: once the tile has landed, the slot's previous round is over
       for (int j = nkg; ok && j < n_kv; ++j) {
@@ -444,30 +479,38 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
         for (int c = 0; c < 64; ++c)
           if (kv0 + c >= lim) s[c] = -INFINITY;
       }
-      // row maximum by a tree (eight independent chains)
+      // row maximum: eight independent chains of three-input max
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = s[i];
 #pragma unroll
-      for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int c = 8; c + 16 <= 64; c += 16)  // columns 8 .. 55
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[56 + i]);  // columns 56 .. 63
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                             fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float m_new = fmaxf(m, mx * sc);
       // move the row maximum only when it grew by more than the threshold
       const bool need = j > 0 && m_new > m + kRescaleThreshold;
       const float m_use = (j == 0 || need) ? m_new : m;
       const float alpha = need ? ex2(m - m_new) : 1.f;
+      // exponents s*sc - m in packed pairs; row sum in four packed accumulators
       uint32_t pk[32];
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
-      const float nm = -m_use;
+      const uint64_t sc2 = pack2(sc, sc), nm2 = pack2(-m_use, -m_use);
+      uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sc, nm));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sc, nm));
-        rs4[c & 3] += p0 + p1;
+        float x0, x1;
+        unpack2(ffma2(pack2(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        acc2[c & 3] = fadd2(acc2[c & 3], pack2(p0, p1));
         pk[c] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c + 1
       }
-      l = l * alpha + ((rs4[0] + rs4[1]) + (rs4[2] + rs4[3]));
+      float r0, r1;
+      unpack2(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);
+      l = l * alpha + (r0 + r1);
       m = m_use;
       if (j >= 2) {
         // the PV that read this P buffer (tile j - 2) is done
