@@ -165,3 +165,29 @@ def test_argument_and_device_checks():
     bt = w.block_table.clone()
     bt[1, 0] = 10_000
     run_extend(w, q, cu, bt=bt.to(dev), expect_err=hpc.HPC_DEVCHK_BAD_BLOCK)
+
+
+def test_many_ragged_sequences():
+    # 100 sequences (the tile lookup scans cu_q_lens in chunks of 32), new-token
+    # counts 0..40 with contexts up to 3000, both CTA shapes
+    g = torch.Generator().manual_seed(53)
+    qn = torch.randint(0, 41, (100,), generator=g).tolist()
+    lens = [n + int(torch.randint(0, 3000, (1,), generator=g)) for n in qn]
+    lens = [max(L, 1) for L in lens]
+    w = W.make_workload(_cfg(16, 2), lengths=lens, seed=54)
+    q, cu = W.make_extend_query(w, qn, seed=55)
+    ref_out, ref_lse = _oracle(w, q, cu)
+    for tpc in (1, 2):
+        out, lse = run_extend(w, q, cu, tpc=tpc)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      label=f"100 ragged sequences tiles/CTA {tpc}")
+
+
+def test_extend_over_long_context():
+    # 16 new tokens after 65520 cached ones: 1024 K/V tiles per CTA
+    w = W.make_workload(_cfg(64, 8), lengths=[65536], seed=56)
+    q, cu = W.make_extend_query(w, [16], seed=57)
+    out, lse = run_extend(w, q, cu)
+    ref_out, ref_lse = _oracle(w, q, cu)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                  label="extend 16 over 65536")
