@@ -130,3 +130,39 @@ def test_host_unit_plans_match_oracle(lib):
             assert np.array_equal(got, ref), (lens[:8], sms, u)
         assert np.array_equal(hpc.hpc_decode_plan_compute_ex(lens, sms, 1),
                               hpc.hpc_decode_plan_compute(lens, sms))
+
+
+def test_extend_argument_statuses(lib):
+    # hpc_extend_attn validates shapes, dtypes and strides before it touches a
+    # device, so host tensors (never dereferenced) exercise every refusal here
+    import torch
+
+    def args(hq=16, hkv=2, d=128, kv_dtype=torch.bfloat16, cu_len=3, total=10):
+        q = torch.zeros(total, hq, d, dtype=torch.bfloat16)
+        kc = torch.zeros(4, hkv, 64, d, dtype=kv_dtype)
+        return [q, kc, kc.clone(), torch.zeros(2, 4, dtype=torch.int32),
+                torch.tensor([8, 6], dtype=torch.int32),
+                torch.tensor([0, 4, 10][:cu_len] + [10] * max(0, cu_len - 3), dtype=torch.int32),
+                torch.zeros(total, hq, d, dtype=torch.bfloat16)]
+
+    def status(a, **kw):
+        try:
+            hpc.hpc_extend_attn(*a, stream=0, **kw)  # an explicit null stream: no torch.cuda
+        except hpc.HpcError as e:
+            return e.status
+        return hpc.HPC_OK
+
+    assert status(args(), tiles_per_cta=3) == hpc.HPC_ERR_INVALID_ARG
+    assert status(args(kv_dtype=torch.uint8)) == hpc.HPC_ERR_UNSUPPORTED   # fp8 cache
+    assert "bf16 cache" in hpc.hpc_last_error()
+    assert status(args(hq=12, hkv=2)) == hpc.HPC_ERR_UNSUPPORTED           # group != 8
+    assert status(args(d=64)) == hpc.HPC_ERR_UNSUPPORTED                   # head_dim
+    assert status(args(cu_len=2)) == hpc.HPC_ERR_INVALID_ARG               # cu_q_lens [B+1]
+    a = args()
+    a[6] = torch.zeros(10, 16, 64, dtype=torch.bfloat16)                    # out shape
+    assert status(a) == hpc.HPC_ERR_INVALID_ARG
+    a = args()
+    a[0] = a[0].float()                                                     # q dtype
+    assert status(a) == hpc.HPC_ERR_INVALID_ARG
+    assert lib.hpc_extend_attn(None, None, None, None, None, None, None, None,
+                               ctypes.c_float(-1.0), None, None) == hpc.HPC_ERR_INVALID_ARG
