@@ -69,7 +69,8 @@ def parse_args():
                     help="skip the device-to-device copy bandwidth probe")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill / extend (tcgen05) timings")
-    ap.add_argument("--prefill-cases", default="q512_prefill,prefill_4x4096,extend_8x(8192+512)",
+    ap.add_argument("--prefill-cases",
+                    default="q512_prefill,prefill_4x4096,extend_8x(8192+512),prefill_4x4096_fp8",
                     help="prefill / extend cases to time (comma list)")
     ap.add_argument("--scale-lengths", type=float, default=1.0,
                     help="scale every KV length of the config (smaller profiling cases)")
@@ -632,15 +633,16 @@ def run_hpc(args, ws, rank, local):
     # ---- prefill / extend attention (tcgen05), the pages' prefill shapes
     if not args.no_prefill and rank == 0:
         peak_tf, peak_src = measured_peak_bf16_tflops()
-        cases = [("q512_prefill", [512], [512]),
-                 ("prefill_4x4096", [4096] * 4, [4096] * 4),
-                 ("extend_8x(8192+512)", [8704] * 8, [512] * 8)]
+        cases = [("q512_prefill", [512], [512], "bf16"),
+                 ("prefill_4x4096", [4096] * 4, [4096] * 4, "bf16"),
+                 ("extend_8x(8192+512)", [8704] * 8, [512] * 8, "bf16"),
+                 ("prefill_4x4096_fp8", [4096] * 4, [4096] * 4, "fp8_e4m3")]
         pf = {}
-        cfgp = W.Config(90, "prefill", 64, 8, "bf16")
         wanted = [c.strip() for c in args.prefill_cases.split(",") if c.strip()]
-        for name, lens, qn in cases:
+        for name, lens, qn, kvd in cases:
             if name not in wanted:
                 continue
+            cfgp = W.Config(90, "prefill", 64, 8, kvd)
             wp = W.make_workload(cfgp, lengths=lens, seed=9000)
             qp, cup = W.make_extend_query(wp, qn, seed=9001)
             qd, kd, vd = qp.to(dev), wp.k_cache.to(dev), wp.v_cache.to(dev)
@@ -651,7 +653,7 @@ def run_hpc(args, ws, rank, local):
 
             def ext():
                 hpc.hpc_extend_attn(qd, kd, vd, btd, sld, cud, od, ld, device_error=errd,
-                                    stream=stream)
+                                    stream=stream, k_scale=wp.k_scale, v_scale=wp.v_scale)
 
             for _ in range(3):
                 flush_l2()
@@ -668,14 +670,14 @@ def run_hpc(args, ws, rank, local):
             us = statistics.mean(a.elapsed_time(b_) for a, b_ in es) * 1e3
             fl = extend_flops(lens, qn, 64)
             tf = fl / (us * 1e-6) / 1e12
-            pf[name] = {"us": round(us, 2), "flops": fl, "tflops": round(tf, 1),
+            pf[name] = {"us": round(us, 2), "flops": fl, "tflops": round(tf, 1), "kv": kvd,
                         "frac_of_bf16_peak": round(tf / peak_tf, 4),
                         "new_tokens": sum(qn), "kv_tokens": sum(lens)}
             line["gpu_launches"] += len(es)
             del qd, kd, vd, od, ld
         pf["peak_tflops"] = peak_tf
         pf["peak_source"] = peak_src
-        pf["note"] = ("hpc_extend_attn, 64 q / 8 kv heads, d128, bf16 cache; useful causal "
+        pf["note"] = ("hpc_extend_attn, 64 q / 8 kv heads, d128, bf16 or e4m3 cache; useful causal "
                       "FLOPs (4*128*H_q per visible key and query row) / CUDA-event time, "
                       "L2 flushed between launches")
         line["prefill"] = pf

@@ -359,8 +359,9 @@ hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in
  *   q           device bf16 [total_q][H_q][128], ragged: the rows of sequence
  *               b start at cu_q_lens[b]; innermost stride 1, other strides
  *               multiples of 8 elements, base 16-byte aligned
- *   k_cache, v_cache, block_table: as hpc_decode_attn, but bf16 only (an
- *               fp8_e4m3 cache gives HPC_ERR_UNSUPPORTED)
+ *   k_cache, v_cache, block_table: as hpc_decode_attn (bf16, or fp8_e4m3
+ *               with per-tensor scales in the descriptors; e4m3 tiles are
+ *               widened exactly to bf16 on the chip before the MMAs)
  *   seq_lens    device int32 [B], L_b >= n_b (else HPC_DEVCHK_BAD_LENGTH and
  *               that sequence's rows are not written)
  *   cu_q_lens   device int32 [B+1], non-decreasing, cu_q_lens[0] = 0,

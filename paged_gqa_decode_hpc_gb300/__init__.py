@@ -338,15 +338,16 @@ def hpc_rope_norm_kv_write(q_in, k_in, v_in, seq_lens, block_table, q_norm_weigh
 
 def hpc_extend_attn(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, lse=None,
                     softmax_scale: Optional[float] = None, device_error=None, stream=None,
-                    tiles_per_cta: int = 0):
+                    tiles_per_cta: int = 0, k_scale: float = 1.0, v_scale: float = 1.0):
     """Prefill / extend attention on the tensor cores: q and out are bf16
     [total_q][H_q][128] with the new tokens of sequence b in rows
     cu_q_lens[b] .. cu_q_lens[b+1]-1 (the last positions of its cache);
     lse f32 [total_q][H_q] or None; device_error an int32 CUDA tensor
     receiving HPC_DEVCHK_* bits, or None; tiles_per_cta 0 (automatic), 1 or 2
-    query tiles of 128 rows per CTA."""
+    query tiles of 128 rows per CTA; k_scale / v_scale the per-tensor scales of
+    an e4m3 cache (uint8 / float8_e4m3fn bytes)."""
     lib = load_library()
-    tq, tk, tv = make_tensor(q), make_tensor(k_cache), make_tensor(v_cache)
+    tq, tk, tv = make_tensor(q), make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
     tb, ts, tc = make_tensor(block_table), make_tensor(seq_lens), make_tensor(cu_q_lens)
     to, tl = make_tensor(out), make_tensor(lse)
     ref = lambda d: ctypes.byref(d) if d is not None else None

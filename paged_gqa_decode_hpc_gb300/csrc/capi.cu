@@ -880,8 +880,9 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   if (k_cache->dtype != v_cache->dtype ||
       (k_cache->dtype != HPC_BF16 && k_cache->dtype != HPC_FP8_E4M3))
     return fail(HPC_ERR_INVALID_ARG, "k_cache/v_cache must both be bf16 or both fp8_e4m3");
-  if (k_cache->dtype != HPC_BF16)
-    return fail(HPC_ERR_UNSUPPORTED, "prefill / extend attention reads a bf16 cache only");
+  const bool fp8 = k_cache->dtype == HPC_FP8_E4M3;
+  if (fp8 && (!std::isfinite(k_cache->scale) || !std::isfinite(v_cache->scale)))
+    return fail(HPC_ERR_INVALID_ARG, "FP8 scales must be finite");
   for (int i = 0; i < 4; ++i)
     if (k_cache->shape[i] != v_cache->shape[i] || k_cache->stride[i] != v_cache->stride[i])
       return fail(HPC_ERR_INVALID_ARG, "k_cache and v_cache must have the same shape and strides");
@@ -906,8 +907,9 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
       !aligned(q->data, 16) || !aligned(out->data, 16))
     return fail(HPC_ERR_INVALID_ARG, "q/out must be 16-byte aligned with strides of 8 elements");
+  const int64_t ce = fp8 ? 1 : 2;
   for (int i = 0; i < 3; ++i)
-    if ((k_cache->stride[i] * 2) % 16)
+    if ((k_cache->stride[i] * ce) % 16)
       return fail(HPC_ERR_INVALID_ARG, "cache strides must be multiples of 16 bytes");
   if (!aligned(k_cache->data, 16) || !aligned(v_cache->data, 16))
     return fail(HPC_ERR_INVALID_ARG, "cache base addresses must be 16-byte aligned");
@@ -940,8 +942,8 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
     return fail(HPC_ERR_UNSUPPORTED, "too many query tiles in one call (split the batch)");
   CUtensorMap tq, tk, tv;
   if ((st = make_q_map(q, &tq)) != HPC_OK) return st;
-  if ((st = make_kv_map(k_cache, false, swap, &tk)) != HPC_OK) return st;
-  if ((st = make_kv_map(v_cache, false, swap, &tv)) != HPC_OK) return st;
+  if ((st = make_kv_map(k_cache, fp8, swap, &tk)) != HPC_OK) return st;
+  if ((st = make_kv_map(v_cache, fp8, swap, &tv)) != HPC_OK) return st;
   ExtendParams p;
   std::memset(&p, 0, sizeof p);
   p.block_table = (const int32_t*)block_table->data;
@@ -961,7 +963,9 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   p.l_st = has_lse ? lse->stride[0] : 0;
   p.l_sh = has_lse ? lse->stride[1] : 0;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
-  p.score_scale_log2 = scale * 1.4426950408889634f;
+  p.kv_fp8 = fp8;
+  p.score_scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_cache->scale : 1.0f);
+  p.v_scale = fp8 ? v_cache->scale : 1.0f;
   p.err = device_error;
   p.timeout_ns = wait_limit_ns();
   cudaError_t e = launch_extend(p, tq, tk, tv, (int)tiles, tiles_per_cta, (cudaStream_t)stream);

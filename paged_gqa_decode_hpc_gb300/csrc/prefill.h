@@ -25,7 +25,9 @@ struct ExtendParams {
   int64_t o_st, o_sh;           // element strides over token, head
   float* lse;                   // [total_q][H_q] or null
   int64_t l_st, l_sh;
-  float score_scale_log2;       // softmax_scale * log2(e)
+  int32_t kv_fp8;               // cache bytes are e4m3 (else bf16)
+  float score_scale_log2;       // softmax_scale * log2(e) (* k_scale for e4m3)
+  float v_scale;                // e4m3 V scale (1 for bf16)
   int32_t* err;                 // device flag word (HPC_DEVCHK_*) or null
   unsigned long long timeout_ns;
 };

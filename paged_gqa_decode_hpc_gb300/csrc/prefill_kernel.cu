@@ -32,6 +32,7 @@
 //    roles stop issuing, and the CTA drains its copies and MMAs and frees its
 //    tensor memory before leaving. No trap, no assert.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "hpc_decode.h"
 #include "prefill.h"
@@ -48,6 +49,8 @@ constexpr int kGroupRows = 8;      // query heads per KV head
 constexpr uint32_t kQBytes = kRows * 128 * 2;         // 32 KB: two 16 KB column halves
 constexpr uint32_t kKVTileBytes = 64 * 128 * 2;       // 16 KB: two 8 KB column halves
 constexpr uint32_t kStageBytes = 2 * kKVTileBytes;    // K + V
+constexpr uint32_t kKVTileBytes8 = 64 * 128;          // 8 KB: one e4m3 K or V tile
+constexpr uint32_t kStageBytes8 = 2 * kKVTileBytes8;  // e4m3 K + V
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -55,16 +58,23 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // the softmax warpgroups (warpgroup g owns tile g: rows = TMEM lanes of its
 // own S and O columns), then one TMA producer warp and one MMA warp per query
 // tile, so the two tiles' S -> softmax -> P*V chains never wait on each other.
-template <int QT>
+template <int QT, bool FP8>
 struct Layout {
-  static constexpr int kProducerWarp = 4 * QT, kMmaWarp0 = 4 * QT + 1;
-  static constexpr int kThreads = 32 * (5 * QT + 1);
-  static constexpr int kStages = QT == 1 ? 6 : 5;                        // K+V ring depth
+  // FP8 caches: 4 converter warps widen each e4m3 K / V tile to bf16 in place
+  // of the TMA writing bf16 directly
+  static constexpr int kConvWarps = FP8 ? 4 : 0;
+  static constexpr int kConvWarp0 = 4 * QT;
+  static constexpr int kProducerWarp = 4 * QT + kConvWarps, kMmaWarp0 = kProducerWarp + 1;
+  static constexpr int kThreads = 32 * (kMmaWarp0 + QT);
+  static constexpr int kStages = FP8 ? 3 : (QT == 1 ? 6 : 5);            // bf16 K+V ring
+  static constexpr int kStages8 = FP8 ? (QT == 1 ? 6 : 4) : 0;           // e4m3 K+V ring
   static constexpr uint32_t kOffQ = 0;                                   // QT x 32 KB
   static constexpr uint32_t kOffKV = QT * kQBytes;                       // stages x 32 KB
-  static constexpr uint32_t kOffBar = kOffKV + kStages * kStageBytes;
-  // q_full, kv_full[S], kv_empty[S], per tile: s_full, s_free, p_full[2], pv_done[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 7 * QT;
+  static constexpr uint32_t kOffKV8 = kOffKV + kStages * kStageBytes;    // stages8 x 16 KB
+  static constexpr uint32_t kOffBar = kOffKV8 + kStages8 * kStageBytes8;
+  // q_full, kv_full[S], kv_empty[S], kv8_full[S8], kv8_empty[S8],
+  // per tile: s_full, s_free, p_full[2], pv_done[2], drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kStages8 + 7 * QT;
   static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align to 1024
   // tensor memory per query tile: S (64 columns) | P0, P1 (32 each, bf16 pairs) | O (128)
@@ -106,6 +116,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+// Two e4m3 bytes (low byte -> low half) to bf16x2, exactly: e4m3 -> f16 is
+// exact, and every e4m3 value is a bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t x) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(x));
+  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+  return pack_bf16(lo, hi);
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -220,22 +239,24 @@ __device__ __forceinline__ int tile_kv(int L, int n, int t0g) {
 
 namespace {
 
-template <int QT>
-__global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
+template <int QT, bool FP8>
+__global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     extend_kernel(const __grid_constant__ ExtendParams p, const __grid_constant__ CUtensorMap tmq,
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-  using Lt = Layout<QT>;
-  constexpr int S = Lt::kStages;
+  using Lt = Layout<QT, FP8>;
+  constexpr int S = Lt::kStages, S8 = Lt::kStages8;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-B alignment
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + Lt::kOffQ, sKV = base + Lt::kOffKV;
+  const uint32_t sQ = base + Lt::kOffQ, sKV = base + Lt::kOffKV, sKV8 = base + Lt::kOffKV8;
   const uint32_t bars = base + Lt::kOffBar;
   const uint32_t bar_q = bars;
   auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
   auto kv_empty = [&](int s) { return bars + 8u * (1 + S + s); };
-  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 7 * g + k); };
+  auto kv8_full = [&](int s) { return bars + 8u * (1 + 2 * S + s); };
+  auto kv8_empty = [&](int s) { return bars + 8u * (1 + 2 * S + S8 + s); };
+  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 2 * S8 + 7 * g + k); };
   auto s_full = [&](int g) { return gbar(g, 0); };
   auto s_free = [&](int g) { return gbar(g, 1); };
   auto p_full = [&](int g, int i) { return gbar(g, 2 + i); };
@@ -263,8 +284,13 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
     if (lane == 0) {
       mbar_init(bar_q, 1);
       for (int s = 0; s < S; ++s) {
-        mbar_init(kv_full(s), 1);
+        // bf16 tile landed: the TMA's transaction count, or the converter threads
+        mbar_init(kv_full(s), FP8 ? 32 * Lt::kConvWarps : 1);
         mbar_init(kv_empty(s), QT);  // one arrival per query tile's MMA warp
+      }
+      for (int s = 0; s < S8; ++s) {
+        mbar_init(kv8_full(s), 1);
+        mbar_init(kv8_empty(s), 32 * Lt::kConvWarps);
       }
       for (int g = 0; g < QT; ++g) {
         mbar_init(s_full(g), 1);
@@ -331,20 +357,38 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
         for (int u = 0; u < cnt; ++u) {
           const int bk = __shfl_sync(0xffffffffu, blk, u);
           if (lane == 0) {
-            const int j = j0 + u, slot = j % S, round = j / S;
-            const bool ok =
-                round == 0 || wait_bar(kv_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
-            if (ok) {
-              const uint32_t fb = kv_full(slot);
-              const uint32_t dk = sKV + slot * kStageBytes, dv = dk + kKVTileBytes;
-              mbar_expect_tx(fb, kStageBytes);
-              tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk);
-              tma_load_4d(dk + kKVTileBytes / 2, &tmk, fb, 64, c1, c2, bk);
-              tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk);
-              tma_load_4d(dv + kKVTileBytes / 2, &tmv, fb, 64, c1, c2, bk);
-              issued = j + 1;
+            const int j = j0 + u;
+            if (FP8) {
+              // e4m3 tiles (64 rows x 128 bytes, one box each) for the converters
+              const int slot = j % S8, round = j / S8;
+              const bool ok = round == 0 ||
+                              wait_bar(kv8_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
+              if (ok) {
+                const uint32_t fb = kv8_full(slot);
+                const uint32_t dk = sKV8 + slot * kStageBytes8, dv = dk + kKVTileBytes8;
+                mbar_expect_tx(fb, kStageBytes8);
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk);
+                issued = j + 1;
+              } else {
+                stop = 1;
+              }
             } else {
-              stop = 1;
+              const int slot = j % S, round = j / S;
+              const bool ok =
+                  round == 0 || wait_bar(kv_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
+              if (ok) {
+                const uint32_t fb = kv_full(slot);
+                const uint32_t dk = sKV + slot * kStageBytes, dv = dk + kKVTileBytes;
+                mbar_expect_tx(fb, kStageBytes);
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk);
+                tma_load_4d(dk + kKVTileBytes / 2, &tmk, fb, 64, c1, c2, bk);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk);
+                tma_load_4d(dv + kKVTileBytes / 2, &tmv, fb, 64, c1, c2, bk);
+                issued = j + 1;
+              } else {
+                stop = 1;
+              }
             }
           }
           stop = __shfl_sync(0xffffffffu, stop, 0);
@@ -355,11 +399,61 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
     named_bar_sync(1, Lt::kThreads);
     // drain: the last copy issued into each slot has landed
     if (lane == 0) {
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int rounds = (issued - s + S - 1) / S;
-        wait_bar(kv_full(s), (rounds - 1) & 1, s_abort, err, lim_ns, false);
+      constexpr int SR = FP8 ? S8 : S;  // the ring the copies went to
+      for (int s = 0; s < SR && s < issued; ++s) {
+        const int rounds = (issued - s + SR - 1) / SR;
+        wait_bar(FP8 ? kv8_full(s) : kv_full(s), (rounds - 1) & 1, s_abort, err, lim_ns, false);
       }
     }
+  } else if (FP8 && warp >= Lt::kConvWarp0 && warp < Lt::kProducerWarp) {
+    // ------------------------------------------- e4m3 -> bf16 converters
+    // Each e4m3 tile (64 token rows x 128 bytes, 128-byte swizzle: 16-byte
+    // chunk c of row t at c ^ (t % 8)) is widened exactly (e4m3 values are
+    // bf16 values) into the bf16 tile the MMAs read: two 64-column halves,
+    // 8-element chunk c' of row t at c' ^ (t % 8). The scales stay out:
+    // k_scale is in the logit scale, v_scale in the epilogue.
+    const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. 127
+    bool ok = n_kv > 0;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s8 = j % S8, sb = j % S;
+      ok = __all_sync(0xffffffffu, wait_bar(kv8_full(s8), (j / S8) & 1, s_abort, err, lim_ns));
+      if (ok && j >= S)
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(kv_empty(sb), ((j / S) - 1) & 1, s_abort, err, lim_ns));
+      if (!ok) break;
+      const uint32_t e8 = sKV8 + s8 * kStageBytes8, kb = sKV + sb * kStageBytes;
+#pragma unroll 2
+      for (int it = 0; it < 8; ++it) {
+        const int item = it * 128 + ct;  // (matrix, row, 16-byte chunk)
+        const int mat = item >> 9, t = (item >> 3) & 63, c = item & 7;
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(e8 + mat * kKVTileBytes8 + t * 128 + ((uint32_t)(c ^ (t & 7)) << 4)));
+        uint32_t w[8];
+        const uint32_t xs[4] = {x0, x1, x2, x3};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[2 * q] = e4m3x2_to_bf16x2((uint16_t)(xs[q] & 0xFFFFu));
+          w[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(xs[q] >> 16));
+        }
+        // elements 16c .. 16c+15 -> half c / 4, 8-element chunks 2(c % 4) and 2(c % 4) + 1
+        const int cc = (c & 3) * 2;
+        const uint32_t row = kb + mat * kKVTileBytes + (c >> 2) * (kKVTileBytes / 2) + t * 128;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row + ((uint32_t)(cc ^ (t & 7)) << 4)),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         row + ((uint32_t)((cc + 1) ^ (t & 7)) << 4)),
+                     "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+      }
+      fence_async_shared();  // the MMAs read the bf16 tile through the async proxy
+      mbar_arrive(kv8_empty(s8));
+      mbar_arrive(kv_full(sb));
+    }
+    named_bar_sync(1, Lt::kThreads);
   } else if (warp >= Lt::kMmaWarp0) {
     // ---------------------------------------------- MMA issue for tile g
     // The whole warp runs the schedule (waits, descriptor arithmetic) so its
@@ -548,7 +642,7 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
       __nv_bfloat16* orow = p.out + (int64_t)(q0 + tok) * p.o_st + (int64_t)head * p.o_sh;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -576,19 +670,19 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, 1)
   }
 }
 
-template <int QT>
+template <int QT, bool FP8>
 cudaError_t launch_qt(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                       const CUtensorMap& tv, int tiles, cudaStream_t stream) {
-  using Lt = Layout<QT>;
+  using Lt = Layout<QT, FP8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(extend_kernel<QT>,
+    cudaError_t e = cudaFuncSetAttribute(extend_kernel<QT, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lt::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  extend_kernel<QT><<<dim3(p.num_kv_heads, tiles), Lt::kThreads, Lt::kSmemBytes, stream>>>(
+  extend_kernel<QT, FP8><<<dim3(p.num_kv_heads, tiles), Lt::kThreads, Lt::kSmemBytes, stream>>>(
       p, tq, tk, tv);
   return cudaGetLastError();
 }
@@ -599,8 +693,12 @@ cudaError_t launch_extend(const ExtendParams& p, const CUtensorMap& tq, const CU
                           const CUtensorMap& tv, int tiles, int tiles_per_cta,
                           cudaStream_t stream) {
   if (tiles <= 0 || p.num_kv_heads <= 0) return cudaSuccess;
-  if (tiles_per_cta == 2) return launch_qt<2>(p, tq, tk, tv, tiles, stream);
-  return launch_qt<1>(p, tq, tk, tv, tiles, stream);
+  if (p.kv_fp8) {
+    if (tiles_per_cta == 2) return launch_qt<2, true>(p, tq, tk, tv, tiles, stream);
+    return launch_qt<1, true>(p, tq, tk, tv, tiles, stream);
+  }
+  if (tiles_per_cta == 2) return launch_qt<2, false>(p, tq, tk, tv, tiles, stream);
+  return launch_qt<1, false>(p, tq, tk, tv, tiles, stream);
 }
 
 }  // namespace hpc

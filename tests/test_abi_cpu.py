@@ -153,8 +153,8 @@ def test_extend_argument_statuses(lib):
         return hpc.HPC_OK
 
     assert status(args(), tiles_per_cta=3) == hpc.HPC_ERR_INVALID_ARG
-    assert status(args(kv_dtype=torch.uint8)) == hpc.HPC_ERR_UNSUPPORTED   # fp8 cache
-    assert "bf16 cache" in hpc.hpc_last_error()
+    assert status(args(kv_dtype=torch.uint8), k_scale=float("inf")) == hpc.HPC_ERR_INVALID_ARG
+    assert "FP8 scales" in hpc.hpc_last_error()
     assert status(args(hq=12, hkv=2)) == hpc.HPC_ERR_UNSUPPORTED           # group != 8
     assert status(args(d=64)) == hpc.HPC_ERR_UNSUPPORTED                   # head_dim
     assert status(args(cu_len=2)) == hpc.HPC_ERR_INVALID_ARG               # cu_q_lens [B+1]

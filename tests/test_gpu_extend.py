@@ -22,8 +22,8 @@ def _lib():
     hpc.load_library()
 
 
-def _cfg(hq, hkv):
-    return W.Config(95, "extend", hq, hkv, "bf16")
+def _cfg(hq, hkv, fp8=False):
+    return W.Config(95, "extend", hq, hkv, "fp8_e4m3" if fp8 else "bf16")
 
 
 def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err=0, tpc=0):
@@ -36,7 +36,7 @@ def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err
                         w.v_cache.to(dev) if v is None else v,
                         w.block_table.to(dev) if bt is None else bt, w.seq_lens.to(dev),
                         cu.to(dev), out, lse, softmax_scale=softmax_scale, device_error=err,
-                        tiles_per_cta=tpc)
+                        tiles_per_cta=tpc, k_scale=w.k_scale, v_scale=w.v_scale)
     torch.cuda.synchronize()
     assert int(err.item()) == expect_err, f"device check bits {int(err.item())}"
     return out, lse
@@ -45,31 +45,36 @@ def run_extend(w, q, cu, k=None, v=None, bt=None, softmax_scale=None, expect_err
 def _oracle(w, q, cu, rows=None, softmax_scale=None):
     return oracle.paged_extend(q, w.k_cache, w.v_cache, w.block_table, w.seq_lens, cu,
                                num_kv_heads=w.num_kv_heads,
-                               softmax_scale=softmax_scale or w.softmax_scale, rows=rows)
+                               softmax_scale=softmax_scale or w.softmax_scale,
+                               kv_is_fp8=w.kv_dtype == "fp8_e4m3", k_scale=w.k_scale,
+                               v_scale=w.v_scale, rows=rows)
 
 
 CASES = [
-    # (H_q, H_kv, lengths, new tokens per sequence)
-    (8, 1, [64], [64]),                                   # one prefill tile row block
-    (16, 2, [100], [100]),                                # prefill with a ragged tail
-    (64, 8, [512], [512]),                                # q512 prefill
-    (64, 8, [70, 9, 130, 64, 1000], [70, 3, 66, 1, 17]),  # ragged mix of prefill / extend
-    (64, 8, [4096], [100]),                               # extend over a long context
-    (32, 4, [50, 300, 17], [0, 20, 17]),                  # a sequence with no new token
-    (128, 16, [200, 65], [33, 65]),
+    # (H_q, H_kv, lengths, new tokens per sequence, fp8_e4m3 cache)
+    (8, 1, [64], [64], False),                                   # one prefill tile row block
+    (16, 2, [100], [100], False),                                # prefill with a ragged tail
+    (64, 8, [512], [512], False),                                # q512 prefill
+    (64, 8, [70, 9, 130, 64, 1000], [70, 3, 66, 1, 17], False),  # ragged prefill / extend mix
+    (64, 8, [4096], [100], False),                               # extend over a long context
+    (32, 4, [50, 300, 17], [0, 20, 17], False),                  # a sequence with no new token
+    (128, 16, [200, 65], [33, 65], False),
+    (64, 8, [512], [512], True),                                 # q512 prefill, e4m3 cache
+    (16, 2, [70, 9, 130, 1000], [70, 3, 66, 17], True),          # ragged mix, e4m3 cache
+    (64, 8, [4096], [100], True),                                # long extend, e4m3 cache
 ]
 
 
-@pytest.mark.parametrize("hq,hkv,lens,qn", CASES)
-def test_matches_oracle(hq, hkv, lens, qn):
-    w = W.make_workload(_cfg(hq, hkv), lengths=lens, seed=40 + len(lens))
+@pytest.mark.parametrize("hq,hkv,lens,qn,fp8", CASES)
+def test_matches_oracle(hq, hkv, lens, qn, fp8):
+    w = W.make_workload(_cfg(hq, hkv, fp8), lengths=lens, seed=40 + len(lens))
     q, cu = W.make_extend_query(w, qn, seed=41)
     ref_out, ref_lse = _oracle(w, q, cu)
     outs = []
     for tpc in (1, 2):  # one or two 128-row query tiles per CTA
         out, lse = run_extend(w, q, cu, tpc=tpc)
         assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
-                      label=f"extend {lens} {qn} tiles/CTA {tpc}")
+                      label=f"extend {lens} {qn} fp8={fp8} tiles/CTA {tpc}")
         outs.append((out, lse))
     # the CTA shape changes which rows share a CTA, not any row's arithmetic
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
@@ -109,11 +114,12 @@ def test_block_permutation_and_layout_invariance():
     assert torch.equal(out1, out3) and torch.equal(lse1, lse3)
 
 
-def test_large_prefill_sampled_rows():
+@pytest.mark.parametrize("fp8", [False, True])
+def test_large_prefill_sampled_rows(fp8):
     # 4 x 4096-token prefill at the decode configs' head shape: every row finite,
     # 64 sampled rows (first, last and tile edges included) against the oracle
     lens = [4096] * 4
-    w = W.make_workload(_cfg(64, 8), lengths=lens, seed=47)
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=lens, seed=47)
     q, cu = W.make_extend_query(w, lens, seed=48)
     out, lse = run_extend(w, q, cu)   # automatic: two query tiles per CTA at this size
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
@@ -124,7 +130,7 @@ def test_large_prefill_sampled_rows():
                       torch.randint(0, 16384, (56,), generator=g).tolist()))
     ref_out, ref_lse = _oracle(w, q, cu, rows=rows)
     assert_parity(out[rows].double().cpu().numpy(), lse[rows].double().cpu().numpy(), ref_out,
-                  ref_lse, label="prefill 4 x 4096 sampled")
+                  ref_lse, label=f"prefill 4 x 4096 sampled fp8={fp8}")
 
 
 def test_decode_shape_equals_decode_kernel():
@@ -144,11 +150,11 @@ def test_argument_and_device_checks():
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
     args = [q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_table.to(dev),
             w.seq_lens.to(dev), cu.to(dev), out]
-    # an fp8 cache is not supported by this kernel
+    # an fp8 cache needs finite per-tensor scales
     k8 = torch.zeros(w.k_cache.shape, dtype=torch.uint8, device=dev)
     with pytest.raises(hpc.HpcError) as e:
-        hpc.hpc_extend_attn(args[0], k8, k8, *args[3:])
-    assert e.value.status == hpc.HPC_ERR_UNSUPPORTED
+        hpc.hpc_extend_attn(args[0], k8, k8, *args[3:], k_scale=float("inf"))
+    assert e.value.status == hpc.HPC_ERR_INVALID_ARG
     with pytest.raises(hpc.HpcError) as e:
         hpc.hpc_extend_attn(*args, tiles_per_cta=3)
     assert e.value.status == hpc.HPC_ERR_INVALID_ARG
