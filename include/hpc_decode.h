@@ -384,7 +384,7 @@ hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
  * caller: tiles_per_cta = 1 (one 128-row query tile of 16 tokens x 8 heads
  * per CTA) or 2 (two tiles, 32 tokens, sharing every K / V tile; the
  * choice for batches that fill the GPU), or 0 for the automatic choice of
- * hpc_extend_attn (2 when ceil(total_q / 32) * H_kv >= 2 * SMs). Results
+ * hpc_extend_attn (2 when ceil(total_q / 32) * H_kv >= SMs / 2). Results
  * are identical either way. Other values give HPC_ERR_INVALID_ARG. */
 hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
                               const hpc_tensor* v_cache, const hpc_tensor* block_table,

@@ -928,12 +928,13 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   if (B > INT32_MAX || total_q > INT32_MAX || NB > INT32_MAX || block_table->shape[1] > INT32_MAX)
     return fail(HPC_ERR_INVALID_ARG, "sizes exceed int32");
   if (tiles_per_cta == 0) {
-    // two 128-row query tiles per CTA when the batch fills the GPU twice over
+    // two 128-row query tiles per CTA (measured as fast or faster from q512
+    // prefill up) unless that leaves more than half of the SMs idle
     int dev = 0, sms = 0;
     HPC_CUDA_TRY(cudaGetDevice(&dev));
     HPC_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     const int64_t pairs = (total_q + 2 * kExtendTileTokens - 1) / (2 * kExtendTileTokens);
-    tiles_per_cta = pairs * Hkv >= 2LL * sms ? 2 : 1;
+    tiles_per_cta = 2 * pairs * Hkv >= sms ? 2 : 1;
   }
   // CTA tiles of T = 16 * tiles_per_cta tokens: sum_b ceil(n_b / T) <= total_q / T + B
   const int64_t tt = (int64_t)kExtendTileTokens * tiles_per_cta;
