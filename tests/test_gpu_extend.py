@@ -197,3 +197,19 @@ def test_extend_over_long_context():
     ref_out, ref_lse = _oracle(w, q, cu)
     assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
                   label="extend 16 over 65536")
+
+
+def test_bench_extend_shape_sampled_rows():
+    # the bench's 8 x (8192 context + 512 new tokens) extend, in the launch
+    # configuration the bench times (automatic CTA shape): 48 sampled rows
+    lens, qn = [8704] * 8, [512] * 8
+    w = W.make_workload(_cfg(64, 8), lengths=lens, seed=9000)
+    q, cu = W.make_extend_query(w, qn, seed=9001)
+    out, lse = run_extend(w, q, cu)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    g = torch.Generator().manual_seed(58)
+    rows = sorted(set([0, 511, 512, 4095, 4096 - 15] +
+                      torch.randint(0, 4096, (43,), generator=g).tolist()))
+    ref_out, ref_lse = _oracle(w, q, cu, rows=rows)
+    assert_parity(out[rows].double().cpu().numpy(), lse[rows].double().cpu().numpy(), ref_out,
+                  ref_lse, label="extend 8 x (8192 + 512) sampled")
