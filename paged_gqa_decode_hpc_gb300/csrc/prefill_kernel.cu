@@ -606,12 +606,10 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       unpack2(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);
       l = l * alpha + (r0 + r1);
       m = m_use;
-      if (j >= 2) {
-        // the PV that read this P buffer (tile j - 2) is done
-        ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, j & 1), ((j - 2) >> 1) & 1, s_abort,
-                                              err, lim_ns));
-        if (!ok) break;
-      }
+      // The P buffer of this tile was last read by P(j-2) V_{j-2}. This query
+      // tile's MMA warp issued that MMA before S(j), and the commit behind
+      // s_full fires only when every MMA the thread issued earlier has
+      // completed: the s_full(j) wait above (and its fence) already ordered it.
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // O is stable once the PV of tile j - 1 is done
         ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, (j - 1) & 1), ((j - 1) >> 1) & 1,
@@ -627,8 +625,6 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
           tmem_st32(trow + kColO + q * 32, o);
         }
-      } else if (j >= 2) {
-        tc_fence_after();
       }
       // P (bf16 pairs) into this tile's tensor-memory buffer: row = lane
       tmem_st32(trow + kColP + 32u * (uint32_t)(j & 1), pk);
