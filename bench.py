@@ -551,12 +551,12 @@ def run_hpc(args, ws, rank, local):
         import oracle
         sample, seqs = oracle_sample(w, budget_s=6.0)
         times = time_oracle(sample, 3)
-        t = statistics.mean(times)
+        t = statistics.median(times)
         line["cpu_baseline"] = {
             "value": round(sample.algorithmic_bytes() / t / 1e9, 4), "unit": "GB/s",
             "cores": oracle.num_cpus(), "kind": "oracle",
             "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
-                      f"{int(w.seq_lens.sum())} KV tokens), mean of 3 runs, {t:.2f} s each"}
+                      f"{int(w.seq_lens.sum())} KV tokens), median of 3 runs, {t:.2f} s"}
 
     # ---- multi-token decode (q_len new tokens per sequence share one KV read)
     if args.q_lens:
