@@ -59,6 +59,8 @@ def parse_args():
                     help="split counts timed for the static ablation ('' = rule only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip timing the step replayed from a CUDA graph")
     ap.add_argument("--no-flush", action="store_true", help="do not flush L2 between steps")
     ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--q-lens", default="2,4",
@@ -490,6 +492,40 @@ def run_hpc(args, ws, rank, local):
             "static_rule_us": round(st_us, 2), "static_sweep_us": sweep,
             "speedup_vs_static_rule": round(st_us / dyn_us, 3),
             "speedup_vs_best_static": round(best / dyn_us, 3)}
+
+    # ---- the same step captured once in a CUDA graph and replayed
+    if not args.no_graph:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):  # one call on the capture stream before capturing
+            hpc.hpc_decode_step(q, kc, vc, bt, sl, plan, num_sms, out, lse, stream=gs,
+                                k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            hpc.hpc_decode_step(q, kc, vc, bt, sl, plan, num_sms, out, lse, stream=gs,
+                                k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            flush_l2()
+            graph.replay()
+        eg = [[mk(), mk()] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for a, b_ in eg:
+            flush_l2()
+            a.record(stream)
+            graph.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        if hpc.hpc_decode_plan_status(plan) != 0:
+            raise SystemExit("device checks fired during the graph replays")
+        g_us = statistics.mean(x.elapsed_time(y) for x, y in eg) * 1e3
+        line["graph"] = {"us_per_step": round(g_us, 2),
+                         "gbs": round(nbytes / (g_us * 1e-6) / 1e9, 1),
+                         "note": "hpc_decode_step captured once in a CUDA graph (its two "
+                                 "kernels keep programmatic dependent launch) and replayed"}
+        line["gpu_launches"] += launches_per_step * args.steps
+        del graph
 
     # ---- end to end through the public API, host buffers
     if not args.no_e2e:
