@@ -8,26 +8,31 @@
 // last n_b of which are its new tokens (already written); new token i
 // attends causally to the positions before L_b - n_b + 1 + i. Prefill is
 // n_b = L_b. GQA with 8 query heads per KV head, head_dim 128, 64-token
-// blocks, BF16 cache.
+// blocks, BF16 or FP8-e4m3 cache with per-tensor scales.
 //
 // GB300 design. Unlike decode (8 FLOP per byte, HBM-bound, mma.sync), a
 // tile of 16 new tokens x 8 query heads = 128 query rows shares every K / V
 // tile, so the work is a dense contraction and runs on tcgen05:
-//  * CTA = (KV head, 16-token tile of one sequence); 6 warps: 4 softmax
-//    warps (thread = query row = TMEM lane), 1 TMA producer warp, 1 MMA warp.
+//  * CTA = (KV head, QT tiles of 16 new tokens of one sequence), QT = 1 or 2.
+//    Warps: 4 softmax warps per query tile (thread = query row = TMEM lane),
+//    4 e4m3 -> bf16 converter warps (FP8 caches only), 1 TMA producer warp,
+//    1 MMA warp per query tile (the tiles' pipelines never wait on each other).
 //  * TMA loads Q once (3-D map over [token][head][128], box 16 x 8 x 64,
 //    128-byte swizzle: row t*8+g of the tile is query head g of token t) and
-//    the K / V tiles of the sequence's blocks into a 4-stage ring.
-//  * S_j = Q K_j^T (M 128, N 64, K 128) into tensor memory, two buffers so
-//    the MMA of tile j+1 runs while the softmax warps work on tile j.
-//  * Online softmax in the log2 domain, one row per thread, no shuffles. The
-//    running maximum is only moved (and O rescaled in tensor memory) when a
-//    row's maximum grows by more than 8 (a factor 256): P = 2^(s - m) then
-//    stays below 256, and the final O / l uses one consistent m per row.
-//  * P (bf16) is written to shared memory in the K-major 128-byte-swizzled
-//    layout and O += P V_j (M 128, N 128, K 64) accumulates in tensor memory
-//    (V is the MN-major operand straight from its TMA tile).
-//  * Epilogue: O / l -> bf16 rows of out, lse = ln 2 * (m + log2 l).
+//    the K / V tiles of the sequence's blocks into a shared-memory ring (for
+//    FP8, into an e4m3 ring that the converters widen into the bf16 ring).
+//  * S_j = Q K_j^T (M 128, N 64, K 128, both operands K-major in shared
+//    memory) into tensor memory; S is single-buffered and S_{j+1} is issued
+//    as soon as the softmax warps have copied S_j out.
+//  * Online softmax in the log2 domain, one row per thread, no shuffles, with
+//    paired f32 math. The running maximum is only moved (and O rescaled in
+//    tensor memory) when a row's maximum grows by more than 8 (a factor 256):
+//    P = 2^(s - m) then stays below 256, and the final O / l uses one
+//    consistent m per row.
+//  * P (bf16 pairs) goes back to tensor memory (double-buffered) and
+//    O += P V_j (M 128, N 128, K 64) reads A = P from tensor memory and V as
+//    the MN-major operand of its tile; O accumulates in tensor memory.
+//  * Epilogue: O * v_scale / l -> bf16 rows of out, lse = ln 2 (m + log2 l).
 //  * Every wait is bounded (globaltimer); a timeout sets the error bit, all
 //    roles stop issuing, and the CTA drains its copies and MMAs and frees its
 //    tensor memory before leaving. No trap, no assert.
