@@ -9,7 +9,8 @@
 // "Attention Backend: Dynamic Load-Balanced Scheduling") but print no merge;
 // this is the standard identity that makes the split softmax exact.
 //
-// One CTA of 4 warps per (sequence, query head). A warp takes every 4th
+// One CTA of 4 warps per (sequence, query head), the heads of a sequence
+// adjacent in the launch order. A warp takes every 4th
 // partial; per round of up to 32 partials each lane loads one partial's
 // (m, l) while the first 8 o rows are fetched alongside (each lane owns 4 of
 // the 128 columns), so a round of up to 8 partials costs one memory round
@@ -45,8 +46,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) merge_kernel(const MergeP
   __shared__ float4 s_o[kMergeWarps][32];
   __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
   griddep_wait();  // partials come from the attention kernel
-  // blockIdx.y = t * H_q + j: query token t, query head j
-  const int b = blockIdx.x, jv = blockIdx.y;
+  // CTA = (sequence b, jv = t * H_q + j: query token t, query head j), jv
+  // fastest: the CTAs of one sequence launch together, so a long sequence's
+  // many-partial merges start in the first wave instead of being spread over
+  // the launch order
+  const int b = (int)(blockIdx.y + blockIdx.z * gridDim.y), jv = (int)blockIdx.x;
+  if (b >= p.num_seqs) return;  // past the last sequence (batches of more than 65535)
   const int t = jv / p.num_q_heads, j = jv % p.num_q_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s0 = p.plan[p.seq_off + b], s1 = p.plan[p.seq_off + b + 1];
@@ -143,7 +148,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) merge_kernel(const MergeP
 cudaError_t launch_merge(const MergeParams& p, int32_t /*num_kv_heads*/, cudaStream_t stream) {
   if (p.num_seqs == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_seqs, p.q_len * p.num_q_heads);
+  // x = query token x head (fastest in the launch order), y (and z beyond
+  // 65535 sequences) = sequence
+  const unsigned gy = p.num_seqs < 65535 ? (unsigned)p.num_seqs : 65535u;
+  cfg.gridDim = dim3((unsigned)(p.q_len * p.num_q_heads), gy, (p.num_seqs + gy - 1) / gy);
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
