@@ -355,7 +355,7 @@ hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in
  * already in its cache as its last n_b positions of L_b = seq_lens[b]; new
  * token i attends to positions 0 .. L_b - n_b + i (causal). Prefill is
  * n_b = L_b, decode n_b = 1. Runs on the tcgen05 tensor cores, one CTA per
- * (KV head, 16 new tokens of one sequence).
+ * (KV head, 16 or 32 new tokens of one sequence; see hpc_extend_attn_ex).
  *   q           device bf16 [total_q][H_q][128], ragged: the rows of sequence
  *               b start at cu_q_lens[b]; innermost stride 1, other strides
  *               multiples of 8 elements, base 16-byte aligned
@@ -370,9 +370,10 @@ hpc_status hpc_rope_norm_kv_write(const hpc_tensor* q_in, const hpc_tensor* k_in
  *   lse         device f32 [total_q][H_q] natural-log LSE (written), or NULL
  *   softmax_scale  > 0, or <= 0 for 1/sqrt(128)
  *   device_error   optional device int32 receiving HPC_DEVCHK_* bits
- * Requirements: H_q == 8 * H_kv, head_dim 128, 64-token blocks, at most
- * 65535 - B 16-token tiles per call (else HPC_ERR_UNSUPPORTED). Allocates
- * nothing; never synchronises the stream.
+ * Requirements: H_q == 8 * H_kv, head_dim 128, 64-token blocks, and
+ * ceil(total_q / T) + B <= 65535 with T = 16 or 32 the CTA's new tokens
+ * (else HPC_ERR_UNSUPPORTED). Allocates nothing; never synchronises the
+ * stream.
  */
 hpc_status hpc_extend_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
                            const hpc_tensor* v_cache, const hpc_tensor* block_table,
