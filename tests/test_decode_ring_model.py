@@ -13,6 +13,8 @@ import random
 
 import pytest
 
+WAIT = "wait"  # yielded by a role that is spinning on a barrier (not progress)
+
 
 class Barrier:
     def __init__(self, name, count):
@@ -56,7 +58,7 @@ class Ring:
         for g in range(self.N):
             slot, par = g % self.S, ((g // self.S) & 1) ^ 1
             while not self.empty[slot].ready(par, phase=g // self.S - 1 if g >= self.S else None):
-                yield
+                yield WAIT
             old = g - self.S
             assert old < 0 or not self.readers.get(old), "slot refilled before its consumers"
             self.readers[g] = set(self.consumers(g))
@@ -74,9 +76,9 @@ class Ring:
             slot = g % self.S
             if self.check_issued:
                 while self.issued[slot] != g:
-                    yield
+                    yield WAIT
             while not self.full[slot].ready((g // self.S) & 1, phase=g // self.S):
-                yield
+                yield WAIT
             assert self.data[slot] == g, "consumer read a slot holding another unit"
             for _ in range(self.rng.randint(0, 4)):
                 yield
@@ -102,8 +104,7 @@ class Ring:
             self.rng.shuffle(roles)
             for r in list(roles[: self.rng.randint(1, len(roles))] if roles else []):
                 try:
-                    next(r)
-                    progressed = True
+                    progressed |= next(r) is not WAIT
                 except StopIteration:
                     roles.remove(r)
                     progressed = True
@@ -137,3 +138,14 @@ def test_parity_alone_is_not_enough():
             caught = True
             break
     assert caught
+
+
+def test_ring_model_reports_a_deadlock():
+    # a consumer waiting for a unit the producer never issues must end the
+    # run with the deadlock report, not spin forever
+    class Stuck(Ring):
+        def consumer(self, w):
+            while self.issued[0] != -1:
+                yield WAIT
+    with pytest.raises(AssertionError, match="deadlock"):
+        Stuck(random.Random(1), 6, 8, 1, 1, 4).run()
