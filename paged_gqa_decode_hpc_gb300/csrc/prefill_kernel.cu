@@ -174,31 +174,31 @@ struct TileInfo {
 // Warp-cooperative: map tile index y (heaviest first) to (sequence, tile).
 // Every sequence contributes ceil(n_b / tile_tokens) tiles; tiles are numbered in
 // sequence order and y counts from the last one, so the CTAs launched first
-// take the tiles that see the most keys.
+// take the tiles that see the most keys. Each lane loads its sequence's row
+// offset, new-token count and length together (independent loads), so up to
+// 32 sequences cost one memory round trip and the found sequence's values
+// come from a shuffle, not from a second, dependent load.
 __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane, int tile_tokens) {
   TileInfo ti;
   ti.valid = 0;
   const int B = p.num_seqs;
-  int total = 0;
-  for (int c = 0; c < B; c += 32) {
+  int q0 = 0, n = 0, L = 0;
+  auto lane_seq = [&](int c) -> int {  // tiles of sequence c + lane
     const int b = c + lane;
-    int nt = 0;
+    q0 = n = L = 0;
     if (b < B) {
-      const int n = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
-      nt = n > 0 ? (n + tile_tokens - 1) / tile_tokens : 0;
+      q0 = p.cu_q_lens[b];
+      n = p.cu_q_lens[b + 1] - q0;
+      L = p.seq_lens[b];
     }
-    total += warp_sum_i(nt);
-  }
-  if (y >= total) return ti;
-  const int gx = total - 1 - y;
+    return n > 0 ? (n + tile_tokens - 1) / tile_tokens : 0;
+  };
+  int total = 0;
+  if (B > 32)  // several chunks: the total first (one chunk: its own sum)
+    for (int c = 0; c < B; c += 32) total += warp_sum_i(lane_seq(c));
   int base = 0;
   for (int c = 0; c < B; c += 32) {
-    const int b = c + lane;
-    int nt = 0;
-    if (b < B) {
-      const int n = p.cu_q_lens[b + 1] - p.cu_q_lens[b];
-      nt = n > 0 ? (n + tile_tokens - 1) / tile_tokens : 0;
-    }
+    const int nt = lane_seq(c);
     int incl = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -206,6 +206,9 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane, int tile_t
       if (lane >= o) incl += v;
     }
     const int chunk = __shfl_sync(0xffffffffu, incl, 31);
+    if (B <= 32) total = chunk;
+    if (y >= total) return ti;
+    const int gx = total - 1 - y;
     if (gx < base + chunk) {
       const unsigned hit = __ballot_sync(0xffffffffu, gx < base + incl);
       const int f = __ffs(hit) - 1;
@@ -213,15 +216,15 @@ __device__ TileInfo find_tile(const ExtendParams& p, int y, int lane, int tile_t
       const int nt_f = __shfl_sync(0xffffffffu, nt, f);
       ti.b = c + f;
       ti.t0 = (gx - (base + incl_f - nt_f)) * tile_tokens;
+      ti.q0 = __shfl_sync(0xffffffffu, q0, f);
+      ti.n = __shfl_sync(0xffffffffu, n, f);
+      ti.L = __shfl_sync(0xffffffffu, L, f);
       ti.valid = 1;
       break;
     }
     base += chunk;
   }
   if (!ti.valid) return ti;
-  ti.q0 = p.cu_q_lens[ti.b];
-  ti.n = p.cu_q_lens[ti.b + 1] - ti.q0;
-  ti.L = p.seq_lens[ti.b];
   if (ti.L < ti.n) {  // more new tokens than positions
     if (lane == 0 && p.err) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
     ti.valid = 0;
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   using Lt = Layout<QT, FP8>;
   constexpr int S = Lt::kStages, S8 = Lt::kStages8;
+  constexpr int S8n = S8 > 0 ? S8 : 1;  // e4m3 ring positions (the ring exists for FP8 only)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1024-B alignment
@@ -365,7 +369,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
             const int j = j0 + u;
             if (FP8) {
               // e4m3 tiles (64 rows x 128 bytes, one box each) for the converters
-              const int slot = j % S8, round = j / S8;
+              const int slot = j % S8n, round = j / S8n;
               const bool ok = round == 0 ||
                               wait_bar(kv8_empty(slot), (round - 1) & 1, s_abort, err, lim_ns);
               if (ok) {
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     named_bar_sync(1, Lt::kThreads);
     // drain: the last copy issued into each slot has landed
     if (lane == 0) {
-      constexpr int SR = FP8 ? S8 : S;  // the ring the copies went to
+      constexpr int SR = FP8 ? S8n : S;  // the ring the copies went to
       for (int s = 0; s < SR && s < issued; ++s) {
         const int rounds = (issued - s + SR - 1) / SR;
         wait_bar(FP8 ? kv8_full(s) : kv_full(s), (rounds - 1) & 1, s_abort, err, lim_ns, false);
@@ -420,8 +424,8 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. 127
     bool ok = n_kv > 0;
     for (int j = 0; ok && j < n_kv; ++j) {
-      const int s8 = j % S8, sb = j % S;
-      ok = __all_sync(0xffffffffu, wait_bar(kv8_full(s8), (j / S8) & 1, s_abort, err, lim_ns));
+      const int s8 = j % S8n, sb = j % S;
+      ok = __all_sync(0xffffffffu, wait_bar(kv8_full(s8), (j / S8n) & 1, s_abort, err, lim_ns));
       if (ok && j >= S)
         ok = __all_sync(0xffffffffu,
                         wait_bar(kv_empty(sb), ((j / S) - 1) & 1, s_abort, err, lim_ns));
@@ -645,14 +649,16 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
       __nv_bfloat16* orow = p.out + (int64_t)(q0 + tok) * p.o_st + (int64_t)head * p.o_sh;
+      // O in two rounds of 64 columns: two tensor-memory loads in flight per wait
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float o[32];
-        tmem_ld32(trow + kColO + q * 32, o);
+      for (int q = 0; q < 4; q += 2) {
+        float o[64];
+        tmem_ld32(trow + kColO + q * 32, *reinterpret_cast<float(*)[32]>(&o[0]));
+        tmem_ld32(trow + kColO + q * 32 + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint4 v;
             v.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
             v.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
