@@ -832,9 +832,9 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
 namespace hpc {
 namespace {
 
-// 3-D TMA descriptor over q [total_q][H_q][128] bf16: box = 16 tokens x
-// 8 heads x 64 columns, 128-byte swizzle (one 16 KB half of a 128-row tile).
-hpc_status make_q_map(const hpc_tensor* q, CUtensorMap* map) {
+// 3-D TMA descriptor over q or out [total_q][H_q][128] bf16: box = 16 tokens
+// x 8 heads x 64 columns, 128-byte swizzle (one 16 KB half of a 128-row tile).
+hpc_status make_q_map(const hpc_tensor* q, CUtensorMap* map, const char* what = "q") {
   auto enc = encode_fn();
   if (!enc) return fail(HPC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)q->shape[1], (cuuint64_t)q->shape[0]};
@@ -845,8 +845,8 @@ hpc_status make_q_map(const hpc_tensor* q, CUtensorMap* map) {
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(HPC_ERR_INVALID_ARG,
-                "cuTensorMapEncodeTiled rejected q (error " + std::to_string((int)r) + ")");
+    return fail(HPC_ERR_INVALID_ARG, std::string("cuTensorMapEncodeTiled rejected ") + what +
+                                         " (error " + std::to_string((int)r) + ")");
   return HPC_OK;
 }
 
@@ -941,8 +941,9 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   const int64_t tiles = (total_q + tt - 1) / tt + B;
   if (tiles > 65535)
     return fail(HPC_ERR_UNSUPPORTED, "too many query tiles in one call (split the batch)");
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((st = make_q_map(q, &tq)) != HPC_OK) return st;
+  if ((st = make_q_map(out, &to, "out")) != HPC_OK) return st;  // full tiles leave by TMA
   if ((st = make_kv_map(k_cache, fp8, swap, &tk)) != HPC_OK) return st;
   if ((st = make_kv_map(v_cache, fp8, swap, &tv)) != HPC_OK) return st;
   ExtendParams p;
@@ -969,7 +970,8 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   p.v_scale = fp8 ? v_cache->scale : 1.0f;
   p.err = device_error;
   p.timeout_ns = wait_limit_ns();
-  cudaError_t e = launch_extend(p, tq, tk, tv, (int)tiles, tiles_per_cta, (cudaStream_t)stream);
+  cudaError_t e =
+      launch_extend(p, tq, tk, tv, to, (int)tiles, tiles_per_cta, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(HPC_ERR_CUDA, std::string("extend launch: ") + cudaGetErrorString(e));
   return HPC_OK;

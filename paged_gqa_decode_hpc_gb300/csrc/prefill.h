@@ -35,7 +35,7 @@ struct ExtendParams {
 // grid = (H_kv, tiles): tiles >= the number of (16 * tiles_per_cta)-token
 // tiles of the batch; tiles_per_cta = 1 or 2 query tiles of 128 rows per CTA.
 cudaError_t launch_extend(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int tiles, int tiles_per_cta,
-                          cudaStream_t stream);
+                          const CUtensorMap& tv, const CUtensorMap& to, int tiles,
+                          int tiles_per_cta, cudaStream_t stream);
 
 }  // namespace hpc

@@ -250,7 +250,8 @@ namespace {
 template <int QT, bool FP8>
 __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     extend_kernel(const __grid_constant__ ExtendParams p, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                  const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmo) {
   using Lt = Layout<QT, FP8>;
   constexpr int S = Lt::kStages, S8 = Lt::kStages8;
   constexpr int S8n = S8 > 0 ? S8 : 1;  // e4m3 ring positions (the ring exists for FP8 only)
@@ -315,6 +316,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       prefetch_map(&tmq);
       prefetch_map(&tmk);
       prefetch_map(&tmv);
+      prefetch_map(&tmo);
     }
   } else if (warp == Lt::kMmaWarp0) {
     tmem_alloc(smem_u32(s_tmem), Lt::kTmemCols);
@@ -562,6 +564,9 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     int lim = L - n + 1 + tok;  // keys visible to this row: positions < lim
     if (lim > L) lim = L;
     const int nk = g == 0 ? nkv[0] : nkv[QT - 1];
+    // the tile leaves by TMA when all its 16 tokens are new tokens of this
+    // sequence (see the epilogue); uniform over the warpgroup
+    const bool full = valid && nk > 0 && t0 + kExtendTileTokens * (g + 1) <= n;
     const uint32_t trow = tmem + 256u * g + ((uint32_t)((warp & 3) * 32) << 16);
     const float sc = p.score_scale_log2;
     float m = -INFINITY, l = 0.f;
@@ -645,6 +650,15 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bar(pv_done(g, (nk - 1) & 1), ((nk - 1) >> 1) & 1,
                                             s_abort, err, lim_ns));
     }
+    // A full 16-token tile leaves through shared memory: its Q buffer is free
+    // once the tile's last P V is done (every S MMA of the tile came before
+    // it), the rows go there in the layout of the Q / out tensor maps
+    // (row t*8 + head, 128-byte swizzle), and one thread stores each 64-column
+    // half with TMA. A partial tile's box would cover rows of the next
+    // sequence, so it is stored row by row. `full` is uniform over the
+    // warpgroup, so every thread reaches the staging barrier even when some
+    // warp stopped early.
+    const uint32_t sQg = sQ + g * kQBytes;
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? p.v_scale / l : 0.f;
@@ -656,14 +670,20 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
         tmem_ld32(trow + kColO + q * 32, *reinterpret_cast<float(*)[32]>(&o[0]));
         tmem_ld32(trow + kColO + q * 32 + 32, *reinterpret_cast<float(*)[32]>(&o[32]));
         tmem_wait_ld();
-        if (row_ok) {
+        const uint32_t srow = sQg + (q >> 1) * (kQBytes / 2) + r * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v;
-            v.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-            v.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-            v.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-            v.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+        for (int c = 0; c < 8; ++c) {
+          uint4 v;
+          v.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+          v.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+          v.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+          v.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+          if (full) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             srow + ((uint32_t)(c ^ (r & 7)) << 4)),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          } else if (row_ok) {
             *reinterpret_cast<uint4*>(orow + q * 32 + c * 8) = v;
           }
         }
@@ -672,6 +692,18 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
         p.lse[(int64_t)(q0 + tok) * p.l_st + (int64_t)head * p.l_sh] =
             l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
+    if (full) {
+      fence_async_shared();  // the TMA store reads the rows through the async proxy
+      if (g == 0) named_bar_sync(2, kRows); else named_bar_sync(3, kRows);
+      if (r == 0 && !*s_abort) {
+        // the tile's first row, re-read here rather than held through the loop
+        const volatile int* si = s_info;
+        const int row = si[5] + si[2] + kExtendTileTokens * g;
+        tma_store_3d(&tmo, sQg, 0, kGroupRows * h, row);
+        tma_store_3d(&tmo, sQg + kQBytes / 2, 64, kGroupRows * h, row);
+        bulk_commit_and_wait_read();  // the buffer is read before the CTA retires
+      }
+    }
     tc_fence_before();
     named_bar_sync(1, Lt::kThreads);
   }
@@ -679,7 +711,8 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
 
 template <int QT, bool FP8>
 cudaError_t launch_qt(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                      const CUtensorMap& tv, int tiles, cudaStream_t stream) {
+                      const CUtensorMap& tv, const CUtensorMap& to, int tiles,
+                      cudaStream_t stream) {
   using Lt = Layout<QT, FP8>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -690,22 +723,22 @@ cudaError_t launch_qt(const ExtendParams& p, const CUtensorMap& tq, const CUtens
     attr_set = true;
   }
   extend_kernel<QT, FP8><<<dim3(p.num_kv_heads, tiles), Lt::kThreads, Lt::kSmemBytes, stream>>>(
-      p, tq, tk, tv);
+      p, tq, tk, tv, to);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_extend(const ExtendParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, int tiles, int tiles_per_cta,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tv, const CUtensorMap& to, int tiles,
+                          int tiles_per_cta, cudaStream_t stream) {
   if (tiles <= 0 || p.num_kv_heads <= 0) return cudaSuccess;
   if (p.kv_fp8) {
-    if (tiles_per_cta == 2) return launch_qt<2, true>(p, tq, tk, tv, tiles, stream);
-    return launch_qt<1, true>(p, tq, tk, tv, tiles, stream);
+    if (tiles_per_cta == 2) return launch_qt<2, true>(p, tq, tk, tv, to, tiles, stream);
+    return launch_qt<1, true>(p, tq, tk, tv, to, tiles, stream);
   }
-  if (tiles_per_cta == 2) return launch_qt<2, false>(p, tq, tk, tv, tiles, stream);
-  return launch_qt<1, false>(p, tq, tk, tv, tiles, stream);
+  if (tiles_per_cta == 2) return launch_qt<2, false>(p, tq, tk, tv, to, tiles, stream);
+  return launch_qt<1, false>(p, tq, tk, tv, to, tiles, stream);
 }
 
 }  // namespace hpc
