@@ -33,6 +33,8 @@
 //    O += P V_j (M 128, N 128, K 64) reads A = P from tensor memory and V as
 //    the MN-major operand of its tile; O accumulates in tensor memory.
 //  * Epilogue: O * v_scale / l -> bf16 rows of out, lse = ln 2 (m + log2 l).
+//    A full 16-token tile is staged in its (then free) Q buffer and written
+//    by one TMA store per 64-column half; a partial tile row by row.
 //  * Every wait is bounded (globaltimer); a timeout sets the error bit, all
 //    roles stop issuing, and the CTA drains its copies and MMAs and frees its
 //    tensor memory before leaving. No trap, no assert.
