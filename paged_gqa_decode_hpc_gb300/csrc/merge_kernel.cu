@@ -10,7 +10,8 @@
 // this is the standard identity that makes the split softmax exact.
 //
 // One CTA of 4 warps per (sequence, query head), the heads of a sequence
-// adjacent in the launch order. A warp takes every 4th
+// adjacent in the launch order. A sequence with at most 8 partials is merged
+// by one warp per head, four heads per CTA. Otherwise a warp takes every 4th
 // partial; per round of up to 32 partials each lane loads one partial's
 // (m, l) while the first 8 o rows are fetched alongside (each lane owns 4 of
 // the 128 columns), so a round of up to 8 partials costs one memory round
@@ -29,6 +30,7 @@ namespace hpc {
 namespace {
 
 constexpr int kMergeWarps = 4;
+constexpr int kWarpMerge = 8;  // at most this many partials: one warp per (token, head)
 constexpr float kLn2f = 0.6931471805599453f;
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -69,6 +71,46 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 8) merge_kernel(const MergeP
     return;
   }
   const int64_t hq = (int64_t)p.q_len * p.num_q_heads;  // partial rows per segment
+  if (ns <= kWarpMerge) {
+    // Few partials (every head of the sequence has the same count): one warp
+    // merges one (token, head) alone in one memory round trip, four per CTA
+    // (jv .. jv+3 share the token: H_q is a multiple of 4), and the CTAs of
+    // the other three heads have nothing to do. A batch of short split
+    // sequences then needs a quarter of the merge warps.
+    if ((jv & 3) != 0) return;
+    const int jw = jv + warp, tw = jw / p.num_q_heads, hw = jw % p.num_q_heads;
+    __nv_bfloat16* ow = p.out + (int64_t)b * p.o_sb + (int64_t)tw * p.o_st +
+                        (int64_t)hw * p.o_sh + 4 * lane;
+    const float* ob = p.ws_o + (int64_t)jw * kHeadDim + 4 * lane;
+    float mk = -INFINITY, lk = 0.f;
+    if (lane < ns) {
+      mk = p.ws_m[(s0 + lane) * hq + jw];
+      lk = p.ws_l[(s0 + lane) * hq + jw];
+    }
+    float4 v[kWarpMerge];
+#pragma unroll
+    for (int u = 0; u < kWarpMerge; ++u)
+      v[u] = u < ns ? *reinterpret_cast<const float4*>(ob + (s0 + u) * hq * kHeadDim)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float M = warp_max(mk);
+    const float wk = (M == -INFINITY || mk == -INFINITY) ? 0.f : ptx_ex2(mk - M);
+    const float L = warp_sum(lk * wk);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kWarpMerge; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wk, u);
+      acc.x += w * v[u].x; acc.y += w * v[u].y; acc.z += w * v[u].z; acc.w += w * v[u].w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(ow) = make_uint2(*reinterpret_cast<const uint32_t*>(&lo),
+                                               *reinterpret_cast<const uint32_t*>(&hi));
+    if (p.lse && lane == 0)
+      p.lse[(int64_t)b * p.l_sb + (int64_t)tw * p.l_st + (int64_t)hw * p.l_sh] =
+          L > 0.f ? (M + __log2f(L)) * kLn2f : -INFINITY;
+    return;
+  }
   const float* obase = p.ws_o + (int64_t)jv * kHeadDim + 4 * lane;
   float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
