@@ -213,3 +213,33 @@ def test_bench_extend_shape_sampled_rows():
     ref_out, ref_lse = _oracle(w, q, cu, rows=rows)
     assert_parity(out[rows].double().cpu().numpy(), lse[rows].double().cpu().numpy(), ref_out,
                   ref_lse, label="extend 8 x (8192 + 512) sampled")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_strided_outputs_and_untouched_neighbours(fp8):
+    # out and lse as views with padded heads: a full 16-token tile leaves
+    # through a TMA store over out's own strides, a partial tile row by row,
+    # and nothing outside the views changes (a full tile's box never reaches
+    # the next sequence's rows, a partial tile's rows are never stored as a box)
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=[70, 512, 40], seed=52)
+    q, cu = W.make_extend_query(w, [70, 512, 33], seed=53)
+    ref_out, ref_lse = _oracle(w, q, cu)
+    total, hq = q.shape[0], q.shape[1]
+    dev = "cuda"
+    big = torch.full((total, hq + 8, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    lse_big = torch.full((total, hq + 8), 7.0, dtype=torch.float32, device=dev)
+    out, lse = big[:, 4:4 + hq, :], lse_big[:, 4:4 + hq]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for tpc in (1, 2):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        hpc.hpc_extend_attn(q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev),
+                            w.block_table.to(dev), w.seq_lens.to(dev), cu.to(dev), out, lse,
+                            device_error=err, tiles_per_cta=tpc, k_scale=w.k_scale,
+                            v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      label=f"strided out, tiles/CTA {tpc}")
+        assert torch.all(big[:, :4] == 7) and torch.all(big[:, 4 + hq:] == 7)
+        assert torch.all(lse_big[:, :4] == 7) and torch.all(lse_big[:, 4 + hq:] == 7)

@@ -74,3 +74,14 @@ def test_empty_sequences():
     w = W.make_workload(_cfg(64, 8), lengths=[0, 0], seed=3)
     out, lse = check_against_oracle(w)
     assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("ns", [2, 7, 8, 9, 16])
+def test_merge_at_the_one_warp_path_boundary(ns):
+    # a sequence split into exactly ns segments: up to 8 partials are merged
+    # by one warp per head, more by four warps per head; next to it a second
+    # sequence split into 3
+    w = W.make_workload(_cfg(64, 8), lengths=[64 * ns], seed=11)
+    check_against_oracle(w, num_sms=ns)
+    w = W.make_workload(_cfg(64, 8), lengths=[64 * ns - 5, 192], seed=12)
+    check_against_oracle(w, num_sms=ns + 3)

@@ -173,3 +173,14 @@ def test_step_many_sequences_unit_plan_through_the_planner_kernel():
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label="step 3300 seqs, unit plan")
     assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(lens, hpc.hpc_device_sm_count(), 8))
+
+
+@pytest.mark.parametrize("sms", [5, 8, 9, 13])
+def test_unit_plan_merges_with_partial_head_segments(sms):
+    # 24 (tile, KV head) units over sms parts: segments start and end inside a
+    # tile, so some heads have empty partials, on both sides of the 8-partial
+    # boundary between the merge's one-warp and four-warp paths
+    w = W.make_workload(_cfg(64, 8), lengths=[192], seed=51)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse = run_plan_ex(w, 8, sms)
+    assert_parity(out, lse, ref_out, ref_lse, label=f"unit plan over {sms} parts")
