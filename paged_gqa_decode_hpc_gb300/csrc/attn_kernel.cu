@@ -908,13 +908,12 @@ cudaError_t launch_cfg(const AttnParams& p, const CUtensorMap& tk, const CUtenso
                        int gy, cudaStream_t stream) {
   using Cfg = KernelCfg<FP8, STAGES, NC, COMBINE>;
   auto kern = attn_kernel<FP8, STAGES, NC, COMBINE>;
-  static bool configured = false;  // per instantiation; attribute is per device function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytesFused);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // devices whose copy is configured
+  cudaError_t e = once_per_device(configured, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::kSmemBytesFused);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(gx, gy);
   cfg.blockDim = dim3(Cfg::kThreads);

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include <string>
 
 #include "hpc_decode.h"
@@ -188,5 +190,21 @@ constexpr int32_t kFusedPlanMaxSeqs = 3072;
 cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_t stream);
 
 void set_error(const std::string& msg);
+
+// Runs `set` (a cudaFuncSetAttribute call) once per device for one kernel:
+// kernel attributes belong to each device's copy of the function, so a
+// process that launches on several devices configures each of them. `done`
+// holds one bit per device id (ids >= 64 are configured on every call).
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t>& done, F set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 }  // namespace hpc

@@ -42,6 +42,7 @@
 #include <cuda_fp16.h>
 
 #include "hpc_decode.h"
+#include "hpc_internal.h"
 #include "prefill.h"
 #include "tc05.cuh"
 
@@ -716,14 +717,13 @@ cudaError_t launch_qt(const ExtendParams& p, const CUtensorMap& tq, const CUtens
                       const CUtensorMap& tv, const CUtensorMap& to, int tiles,
                       cudaStream_t stream) {
   using Lt = Layout<QT, FP8>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(extend_kernel<QT, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Lt::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // devices whose copy is configured
+  const cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(extend_kernel<QT, FP8>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Lt::kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   extend_kernel<QT, FP8><<<dim3(p.num_kv_heads, tiles), Lt::kThreads, Lt::kSmemBytes, stream>>>(
       p, tq, tk, tv, to);
   return cudaGetLastError();
