@@ -427,6 +427,14 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     // 8-element chunk c' of row t at c' ^ (t % 8). The scales stay out:
     // k_scale is in the logit scale, v_scale in the epilogue.
     const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. 127
+    // Work item it (0 .. 7) of thread ct: matrix it / 4, row t, 16-byte chunk
+    // c. A 16-byte shared access is served 8 threads at a time; each such
+    // group takes four chunks of one row and the other four of a row of the
+    // opposite swizzle parity, so its e4m3 loads and both of its bf16 stores
+    // (chunks 2(c % 4) and 2(c % 4) + 1 of a half, the halves 8 KB apart on
+    // the same banks) each cover all 8 bank groups: no bank conflict, and no
+    // extra instruction in the loop.
+    const int cq = ct & 15, c = cq & 7, cr = ((cq >> 2) & 1) ^ (cq >> 3);
     bool ok = n_kv > 0;
     for (int j = 0; ok && j < n_kv; ++j) {
       const int s8 = j % S8n, sb = j % S;
@@ -438,8 +446,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       const uint32_t e8 = sKV8 + s8 * kStageBytes8, kb = sKV + sb * kStageBytes;
 #pragma unroll 2
       for (int it = 0; it < 8; ++it) {
-        const int item = it * 128 + ct;  // (matrix, row, 16-byte chunk)
-        const int mat = item >> 9, t = (item >> 3) & 63, c = item & 7;
+        const int mat = it >> 2, t = (it & 3) * 16 + (ct >> 4) * 2 + cr;
         uint32_t x0, x1, x2, x3;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
