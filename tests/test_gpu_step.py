@@ -184,3 +184,15 @@ def test_unit_plan_merges_with_partial_head_segments(sms):
     ref_out, ref_lse = oracle.decode_workload(w)
     out, lse = run_plan_ex(w, 8, sms)
     assert_parity(out, lse, ref_out, ref_lse, label=f"unit plan over {sms} parts")
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform", "skewed_fp8", "random_mixed"])
+def test_step_full_size_configs(name):
+    # the launch configuration bench.py times (hpc_decode_step: the plan built
+    # in the attention kernel's prologue, then the merge), at each config's
+    # full size, element by element against the fp64 oracle
+    w = W.make_workload(name)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label=f"step {name}")
