@@ -42,9 +42,10 @@ unsigned long long wait_limit_ns() {
 }
 
 // Failure-path test switch: with HPC_DECODE_TEST_WITHHOLD_COPIES=1 the
-// attention kernel's producer issues no copies, so every consumer wait runs
-// out (bounded by HPC_DECODE_WAIT_LIMIT_MS) and the step must come back with
-// HPC_DEVCHK_TIMEOUT and a usable context. Read once per process.
+// producers of the attention and extend kernels issue no copies, so every
+// consumer wait runs out (bounded by HPC_DECODE_WAIT_LIMIT_MS) and the call
+// must come back with HPC_DEVCHK_TIMEOUT and a usable context. Read once per
+// process.
 bool withhold_copies() {
   static const bool v = [] {
     const char* s = std::getenv("HPC_DECODE_TEST_WITHHOLD_COPIES");
@@ -970,6 +971,7 @@ extern "C" hpc_status hpc_extend_attn_ex(const hpc_tensor* q, const hpc_tensor* 
   p.v_scale = fp8 ? v_cache->scale : 1.0f;
   p.err = device_error;
   p.timeout_ns = wait_limit_ns();
+  p.withhold_copies = withhold_copies();
   cudaError_t e =
       launch_extend(p, tq, tk, tv, to, (int)tiles, tiles_per_cta, (cudaStream_t)stream);
   if (e != cudaSuccess)

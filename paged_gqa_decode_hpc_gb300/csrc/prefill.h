@@ -30,6 +30,7 @@ struct ExtendParams {
   float v_scale;                // e4m3 V scale (1 for bf16)
   int32_t* err;                 // device flag word (HPC_DEVCHK_*) or null
   unsigned long long timeout_ns;
+  int32_t withhold_copies;      // failure-path test: the producer issues no copy
 };
 
 // grid = (H_kv, tiles): tiles >= the number of (16 * tiles_per_cta)-token

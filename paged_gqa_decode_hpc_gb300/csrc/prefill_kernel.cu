@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
   if (warp == Lt::kProducerWarp) {
     // ------------------------------------------------------------ producer
     int issued = 0;  // K/V tiles whose copies were issued (in order)
-    if (n_kv > 0) {
+    if (n_kv > 0 && !p.withhold_copies) {  // failure-path test: nothing is issued
       if (lane == 0) {
         mbar_expect_tx(bar_q, QT * kQBytes);
 #pragma unroll

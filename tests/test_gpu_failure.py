@@ -1,6 +1,6 @@
-"""Failure detection on the GPU without a fault: the attention kernel's
-bounded waits must end a step whose data never arrives with an error status,
-and leave the context usable.
+"""Failure detection on the GPU without a fault: the bounded waits of the
+attention and extend kernels must end a call whose data never arrives with an
+error status, and leave the context usable.
 
 A child process sets HPC_DECODE_TEST_WITHHOLD_COPIES=1 (the producer warp
 issues no copies, so every consumer waits on a word nothing sets) and a
@@ -46,6 +46,20 @@ for hkv, hq in ((8, 64), (1, 8)):  # without and with the warps' combine step
     bits = hpc.hpc_decode_plan_status(plan)  # synchronises
     res[str(hkv)] = {"bits": bits, "seconds": time.time() - t0}
     plan.destroy()
+# the extend kernel (tcgen05, TMA), BF16 and FP8 caches, one and two query tiles per CTA
+for kvd in ("bf16", "fp8_e4m3"):
+    w = W.make_workload(W.Config(99, "fail", 64, 8, kvd), lengths=[600, 70], seed=72)
+    q, cu = W.make_extend_query(w, [600, 33], seed=73)
+    for tpc in (1, 2):
+        out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        t0 = time.time()
+        hpc.hpc_extend_attn(q.cuda(), w.k_cache.cuda(), w.v_cache.cuda(), w.block_table.cuda(),
+                            w.seq_lens.cuda(), cu.cuda(), out, device_error=err, tiles_per_cta=tpc,
+                            k_scale=w.k_scale, v_scale=w.v_scale)
+        bits = int(err.item())  # synchronises
+        res[f"extend_{kvd}_{tpc}"] = {"bits": bits, "seconds": time.time() - t0}
 # the context still works
 res["usable"] = float(torch.arange(1000, device="cuda", dtype=torch.float32).sum().item()) == 499500.0
 print(json.dumps(res))
@@ -65,9 +79,10 @@ def test_withheld_copies_end_in_a_timeout_status_and_a_usable_context():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    for hkv in ("8", "1"):
-        assert res[hkv]["bits"] & hpc.HPC_DEVCHK_TIMEOUT, res
-        assert res[hkv]["seconds"] < 30, res
+    for key in ("8", "1", "extend_bf16_1", "extend_bf16_2", "extend_fp8_e4m3_1",
+                "extend_fp8_e4m3_2"):
+        assert res[key]["bits"] & hpc.HPC_DEVCHK_TIMEOUT, res
+        assert res[key]["seconds"] < 30, res
     assert res["usable"]
     # and this process, without the switch, still computes the right answer
     w = W.make_workload(W.Config(99, "fail", 64, 8, "bf16"), lengths=[3000, 64, 700], seed=71)
