@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--json-out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--q-lens", default="2,4",
                     help="query-token counts timed for multi-token decode ('' = none)")
+    ap.add_argument("--tc-min-q-len", type=int, default=0,
+                    help="smallest q_len run on the tensor-core decode kernel (0: the "
+                         "library's per-dtype default; 9: never)")
     ap.add_argument("--no-prologue", action="store_true",
                     help="skip timing the fused prologue kernel")
     ap.add_argument("--no-copy-probe", action="store_true",
@@ -596,7 +599,8 @@ def run_hpc(args, ws, rank, local):
 
     # ---- multi-token decode (q_len new tokens per sequence share one KV read)
     if args.q_lens:
-        mt = {}
+        hpc.hpc_decode_tc_min_q_len(args.tc_min_q_len)
+        mt = {"tc_min_q_len": hpc.hpc_decode_tc_min_q_len(-1)}
         for T in [int(x) for x in args.q_lens.split(",") if x.strip()]:
             qm = W.make_multi_query(w, T, seed=8000 + T).to(dev)
             om = torch.empty_like(qm)

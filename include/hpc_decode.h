@@ -220,7 +220,10 @@ void hpc_decode_plan_destroy(hpc_plan_t plan);
  * per-split kernel (static plan), then the log-sum-exp merge of split
  * sequences. Softmax scale 1/sqrt(head_dim).
  *
- *   q            device bf16 [B][H_q][128], innermost stride 1
+ *   q            device bf16 [B][H_q][128], or [B][q_len][H_q][128] for q_len
+ *                (1..8) new tokens per sequence, innermost stride 1. The
+ *                q_len tokens are the last q_len positions of the sequence:
+ *                token t sees positions < seq_lens[b] - (q_len - 1 - t)
  *   k_cache      device bf16 or fp8_e4m3 [num_blocks][H_kv][64][128],
  *   v_cache      innermost stride 1, other strides multiples of 16 bytes, base
  *                16-byte aligned (a [num_blocks][64][H_kv][128] cache passes as
@@ -230,8 +233,14 @@ void hpc_decode_plan_destroy(hpc_plan_t plan);
  *                [b][i] for i < ceil(seq_lens[b]/64) is a physical block id
  *   seq_lens     device int32 [B]: the lengths the plan was built from
  *   plan         from any hpc_decode_plan* call with num_seqs == B
- *   out          device bf16 [B][H_q][128], innermost stride 1 (written)
- *   lse          device f32 [B][H_q] natural-log LSE (written), or NULL
+ *   out          device bf16, q's shape, innermost stride 1 (written)
+ *   lse          device f32 [B][H_q] (or [B][q_len][H_q]) natural-log LSE
+ *                (written), or NULL
+ * With q_len >= the threshold of hpc_decode_tc_min_q_len (by default 4 for
+ * a bf16 cache, 3 for fp8_e4m3) and a
+ * dynamic tile plan, the tile products run on the tcgen05 tensor cores, one
+ * CTA per (KV head, plan part): such a plan is best built with
+ * num_sms / H_kv parts. Otherwise one warp per (token, KV head) runs them.
  * Requirements: H_q == 8 * H_kv and H_kv in {1, 2, 4, 8, 16, 32, 64};
  * head_dim 128; 64-token blocks -- else HPC_ERR_UNSUPPORTED.
  * The first call on a plan from hpc_decode_plan / _static allocates its
@@ -253,8 +262,11 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
  * lengths (hpc_decode_plan_compute_ex, hpc_decode_plan_export): a plan of
  * one unit per (tile, KV head) (units_per_tile = num_kv_heads) when
  * num_kv_heads * q_len <= 8 and num_kv_heads > 1, else of tiles. Batches
- * above 3072 sequences run the separate planner kernel first. Allocates nothing; may be captured in a
- * CUDA graph after a first call outside the capture.
+ * above 3072 sequences run the separate planner kernel first. With q_len at
+ * or above the tensor-core threshold (hpc_decode_tc_min_q_len) the planner
+ * kernel builds a tile plan of max(1, num_sms / num_kv_heads) parts and the
+ * tensor-core kernel runs one CTA per (KV head, part). Allocates nothing; may
+ * be captured in a CUDA graph after a first call outside the capture.
  *   q, k_cache, v_cache, block_table, out, lse: as hpc_decode_attn
  *   seq_lens  device int32 [B], contiguous
  *   plan      from hpc_decode_plan_create with max_seqs >= B
@@ -271,6 +283,20 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
                               const hpc_tensor* v_cache, const hpc_tensor* block_table,
                               const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
                               hpc_tensor* lse, float softmax_scale, void* stream);
+
+/*
+ * hpc_decode_tc_min_q_len -- the smallest q_len for which hpc_decode_attn*
+ * and hpc_decode_step use the tensor-core kernel (process-wide setting).
+ *   q_len     >= 2: the new threshold for both cache dtypes (above 8: the
+ *             path is never used); 0: the defaults (4 with a bf16 cache, 3
+ *             with fp8_e4m3, the measured crossovers); < 0: no change
+ *             (query only); 1: HPC_ERR_INVALID_ARG
+ *   previous  host int32 receiving the setting before the call (0 for the
+ *             defaults), or NULL
+ * Both kernels compute the same attention; the setting moves only the
+ * choice of kernel (tests and benchmarks pin one with it).
+ */
+hpc_status hpc_decode_tc_min_q_len(int32_t q_len, int32_t* previous);
 
 /*
  * hpc_decode_plan_set_timing_events -- instrumentation: while set, each

@@ -25,7 +25,7 @@ __all__ = [
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
     "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc", "hpc_decode_step",
-    "hpc_rope_norm_kv_write", "hpc_extend_attn",
+    "hpc_rope_norm_kv_write", "hpc_extend_attn", "hpc_decode_tc_min_q_len",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
 ]
@@ -103,6 +103,7 @@ def load_library():
             "hpc_decode_plan_set_timing_events": [P, P, P, P],
             "hpc_decode_attn_noalloc": [T, T, T, T, T, i32, T, T, P, P],
             "hpc_decode_step": [T, T, T, T, T, P, i32, T, T, P],
+            "hpc_decode_tc_min_q_len": [i32, pi32],
             "hpc_rope_norm_kv_write": [T, T, T, T, T, T, T, ctypes.c_float, ctypes.c_float,
                                        T, T, T, T, P, P],
             "hpc_extend_attn": [T, T, T, T, T, T, T, T, ctypes.c_float, P, P],
@@ -277,6 +278,15 @@ def hpc_decode_plan_set_timing_events(plan: Plan, ev_start=None, ev_attn_done=No
         return ctypes.c_void_p(int(e.cuda_event if hasattr(e, "cuda_event") else e))
     _check(load_library().hpc_decode_plan_set_timing_events(plan.handle, h(ev_start),
                                                             h(ev_attn_done), h(ev_end)))
+
+
+def hpc_decode_tc_min_q_len(q_len: int = -1) -> int:
+    """Set the smallest q_len that runs on the tensor-core decode kernel
+    (>= 2; above 8: never; 0: the per-dtype defaults, 4 for bf16 and 3 for
+    fp8_e4m3 caches; < 0: no change) and return the previous setting."""
+    prev = ctypes.c_int32()
+    _check(load_library().hpc_decode_tc_min_q_len(int(q_len), ctypes.byref(prev)))
+    return int(prev.value)
 
 
 def hpc_device_sm_count() -> int:

@@ -9,6 +9,7 @@
 #include <string>
 #include <vector>
 
+#include "decode_tc.h"
 #include "hpc_internal.h"
 #include "prefill.h"
 
@@ -52,6 +53,19 @@ bool withhold_copies() {
     return s && s[0] == '1';
   }();
   return v;
+}
+
+// Smallest q_len (new tokens per sequence) that hpc_decode_attn* and
+// hpc_decode_step run on the tensor-core decode kernel (decode_tc_kernel.cu)
+// instead of the one-warp-per-token kernel (attn_kernel.cu); values above
+// kMaxQueryTokens turn the tensor-core path off. 0 selects the measured
+// crossover of each cache dtype: on the skewed 1 x 128K + 31 x 4K batch the
+// tensor-core kernel is faster from q_len 4 with a bf16 cache (170 vs
+// 173 us) and from q_len 3 with an e4m3 cache (159 vs 171 us).
+std::atomic<int32_t> g_tc_min_q_len{0};
+int32_t tc_min_q_len(bool fp8) {
+  const int32_t v = g_tc_min_q_len.load(std::memory_order_relaxed);
+  return v > 0 ? v : (fp8 ? 3 : 4);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -440,6 +454,24 @@ void hpc_decode_plan_destroy(hpc_plan_t plan) {
 
 namespace hpc {
 namespace {
+// 4-D TMA descriptor over q [B][q_len][H_q][128] for the tensor-core decode
+// kernel: box (64 columns, 8 heads, q_len tokens, 1 sequence), 128-byte
+// swizzle. False when the strides do not form such a tensor (the caller then
+// keeps the one-warp-per-token kernel).
+bool make_decode_q_map(const hpc_tensor* q, CUtensorMap* map) {
+  auto enc = encode_fn();
+  if (!enc || q->ndim != 4) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)q->shape[2], (cuuint64_t)q->shape[1],
+                        (cuuint64_t)q->shape[0]};
+  cuuint64_t strides[3] = {(cuuint64_t)q->stride[2] * 2, (cuuint64_t)q->stride[1] * 2,
+                           (cuuint64_t)q->stride[0] * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kGroup, (cuuint32_t)q->shape[1], 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q->data, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Attention + merge. fused_num_sms > 0: the attention kernel plans the step
 // itself (P = min(fused_num_sms, T)) and writes the plan words into `plan`.
 hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_tensor* v_cache,
@@ -604,8 +636,50 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
     p.err = plan->d_err;
     p.timeout_ns = wait_limit_ns();
     p.withhold_copies = withhold_copies();
+    // q_len >= the tensor-core threshold with a tile plan: the q_len x 8 query
+    // rows of a KV head go through tcgen05 (decode_tc_kernel.cu)
+    CUtensorMap tq;
+    const bool tc = multi && T >= tc_min_q_len(fp8) &&
+                    plan->kind == HPC_PLAN_DYNAMIC && plan->units == 1 && fused_num_sms == 0 &&
+                    make_decode_q_map(q, &tq);
     if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
-    cudaError_t ce = launch_attention(p, tk, tv, fp8, gx, gy, s);
+    cudaError_t ce;
+    if (tc) {
+      DecodeTcParams tp;
+      std::memset(&tp, 0, sizeof tp);
+      tp.block_table = p.block_table;
+      tp.bt_sb = p.bt_sb;
+      tp.max_blocks = p.max_blocks;
+      tp.seq_lens = p.seq_lens;
+      tp.plan = plan->d_words;
+      tp.part_off = p.part_off;
+      tp.seg_off = p.seg_off;
+      tp.num_seqs = p.num_seqs;
+      tp.num_q_heads = p.num_q_heads;
+      tp.num_kv_heads = p.num_kv_heads;
+      tp.num_blocks = p.num_blocks;
+      tp.q_len = p.q_len;
+      tp.kv_swap = p.kv_swap;
+      tp.out = p.out;
+      tp.o_sb = p.o_sb;
+      tp.o_st = p.o_st;
+      tp.o_sh = p.o_sh;
+      tp.lse = p.lse;
+      tp.l_sb = p.l_sb;
+      tp.l_st = p.l_st;
+      tp.l_sh = p.l_sh;
+      tp.ws_o = p.ws_o;
+      tp.ws_m = p.ws_m;
+      tp.ws_l = p.ws_l;
+      tp.score_scale_log2 = p.score_scale_log2;
+      tp.v_scale = p.v_scale;
+      tp.err = p.err;
+      tp.timeout_ns = p.timeout_ns;
+      tp.withhold_copies = p.withhold_copies;
+      ce = launch_decode_tc(tp, tq, tk, tv, fp8, gx, s);
+    } else {
+      ce = launch_attention(p, tk, tv, fp8, gx, gy, s);
+    }
     if (ce != cudaSuccess)
       return fail(HPC_ERR_CUDA, std::string("attention launch: ") + cudaGetErrorString(ce));
   }
@@ -667,6 +741,28 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
     return fail(HPC_ERR_INVALID_ARG, "num_seqs exceeds the plan's max_seqs");
   if (num_sms <= 0 || num_sms > plan->layout.cap_parts)
     return fail(HPC_ERR_INVALID_ARG, "num_sms must be in [1, plan num_sms]");
+  // q_len at or above the tensor-core threshold: a tile plan of
+  // num_sms / H_kv parts, one CTA per (KV head, part), built by the planner
+  // kernel.
+  const int64_t Tq = q->ndim == 4 ? q->shape[1] : 1;
+  const bool fp8_cache = k_cache && k_cache->dtype == HPC_FP8_E4M3;
+  if (q->ndim == 4 && Tq >= tc_min_q_len(fp8_cache) && Tq <= kMaxQueryTokens) {
+    const int64_t hkv = (k_cache && k_cache->ndim == 4 && k_cache->shape[1] > 0)
+                            ? k_cache->shape[1] : 1;
+    const int32_t parts = (int32_t)std::max<int64_t>(1, num_sms / hkv);
+    cudaError_t e = launch_plan_device((const int32_t*)seq_lens->data, (int32_t)B, parts,
+                                       plan->d_words, plan->layout, plan->d_err,
+                                       (cudaStream_t)stream, 1);
+    if (e != cudaSuccess)
+      return fail(HPC_ERR_CUDA, std::string("device planner launch: ") + cudaGetErrorString(e));
+    plan->num_seqs = (int32_t)B;
+    plan->num_sms = parts;
+    plan->host_num_parts = -1;
+    plan->host_num_segs = -1;
+    plan->units = 1;
+    return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
+                     0);
+  }
   // One unit per (tile, KV head) when the kernel's warp layout takes all KV
   // heads in one pass with one warp per (head, token): an 8x finer partition.
   int32_t units = 1;
@@ -698,6 +794,14 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
   plan->host_num_segs = -1;
   return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
                    num_sms);
+}
+
+hpc_status hpc_decode_tc_min_q_len(int32_t q_len, int32_t* previous) {
+  if (previous) *previous = g_tc_min_q_len.load(std::memory_order_relaxed);
+  if (q_len < 0) return HPC_OK;
+  if (q_len == 1) return fail(HPC_ERR_INVALID_ARG, "the tensor-core path needs q_len >= 2");
+  g_tc_min_q_len.store(q_len, std::memory_order_relaxed);
+  return HPC_OK;
 }
 
 hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, void* ev_attn_done,

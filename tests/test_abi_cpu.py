@@ -28,7 +28,7 @@ def declared_functions():
     return sorted(set(re.findall(r"\b(hpc_[a-z0-9_]+)\s*\(", text)))
 
 
-def test_header_declares_the_two_north_calls():
+def test_header_declares_the_plan_and_attention_calls():
     names = declared_functions()
     assert "hpc_decode_plan" in names and "hpc_decode_attn" in names
 

@@ -1,5 +1,6 @@
 """Failure detection on the GPU without a fault: the bounded waits of the
-attention and extend kernels must end a call whose data never arrives with an
+attention, tensor-core decode and extend kernels must end a call whose data
+never arrives with an
 error status, and leave the context usable.
 
 A child process sets HPC_DECODE_TEST_WITHHOLD_COPIES=1 (the producer warp
@@ -46,6 +47,23 @@ for hkv, hq in ((8, 64), (1, 8)):  # without and with the warps' combine step
     bits = hpc.hpc_decode_plan_status(plan)  # synchronises
     res[str(hkv)] = {"bits": bits, "seconds": time.time() - t0}
     plan.destroy()
+# the tensor-core multi-token decode kernel (q_len 4), BF16 and FP8 caches
+for kvd in ("bf16", "fp8_e4m3"):
+    w = W.make_workload(W.Config(99, "fail", 64, 8, kvd), lengths=[3000, 64, 700], seed=74)
+    d = device_workload(w)
+    q = W.make_multi_query(w, 4, seed=75).cuda()
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(3, sms, 4 * 64)
+    out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
+    prev = hpc.hpc_decode_tc_min_q_len(2)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    hpc.hpc_decode_step(q, d["k"], d["v"], d["bt"], d["sl"], plan, sms, out,
+                        k_scale=w.k_scale, v_scale=w.v_scale)
+    bits = hpc.hpc_decode_plan_status(plan)  # synchronises
+    hpc.hpc_decode_tc_min_q_len(prev)
+    res[f"tc_{kvd}"] = {"bits": bits, "seconds": time.time() - t0}
+    plan.destroy()
 # the extend kernel (tcgen05, TMA), BF16 and FP8 caches, one and two query tiles per CTA
 for kvd in ("bf16", "fp8_e4m3"):
     w = W.make_workload(W.Config(99, "fail", 64, 8, kvd), lengths=[600, 70], seed=72)
@@ -79,8 +97,8 @@ def test_withheld_copies_end_in_a_timeout_status_and_a_usable_context():
                        capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    for key in ("8", "1", "extend_bf16_1", "extend_bf16_2", "extend_fp8_e4m3_1",
-                "extend_fp8_e4m3_2"):
+    for key in ("8", "1", "tc_bf16", "tc_fp8_e4m3", "extend_bf16_1", "extend_bf16_2",
+                "extend_fp8_e4m3_1", "extend_fp8_e4m3_2"):
         assert res[key]["bits"] & hpc.HPC_DEVCHK_TIMEOUT, res
         assert res[key]["seconds"] < 30, res
     assert res["usable"]
