@@ -228,6 +228,18 @@ hpc_status new_host_plan(const int32_t* words, const PlanLayout& L, int32_t kind
 
 void set_error(const std::string& msg) { g_last_error = msg; }
 
+int32_t decode_plan_parts(const hpc_tensor* q, const hpc_tensor* k_cache, int32_t num_sms,
+                          bool* tensor_core) {
+  const int64_t T = (q && q->ndim == 4) ? q->shape[1] : 1;
+  const bool fp8 = k_cache && k_cache->dtype == HPC_FP8_E4M3;
+  const bool tc = q && q->ndim == 4 && T >= tc_min_q_len(fp8) && T <= kMaxQueryTokens;
+  if (tensor_core) *tensor_core = tc;
+  if (!tc) return num_sms;
+  const int64_t hkv =
+      (k_cache && k_cache->ndim == 4 && k_cache->shape[1] > 0) ? k_cache->shape[1] : 1;
+  return (int32_t)std::max<int64_t>(1, num_sms / hkv);
+}
+
 }  // namespace hpc
 
 using namespace hpc;
@@ -744,12 +756,9 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
   // q_len at or above the tensor-core threshold: a tile plan of
   // num_sms / H_kv parts, one CTA per (KV head, part), built by the planner
   // kernel.
-  const int64_t Tq = q->ndim == 4 ? q->shape[1] : 1;
-  const bool fp8_cache = k_cache && k_cache->dtype == HPC_FP8_E4M3;
-  if (q->ndim == 4 && Tq >= tc_min_q_len(fp8_cache) && Tq <= kMaxQueryTokens) {
-    const int64_t hkv = (k_cache && k_cache->ndim == 4 && k_cache->shape[1] > 0)
-                            ? k_cache->shape[1] : 1;
-    const int32_t parts = (int32_t)std::max<int64_t>(1, num_sms / hkv);
+  bool tensor_core = false;
+  const int32_t parts = decode_plan_parts(q, k_cache, num_sms, &tensor_core);
+  if (tensor_core) {
     cudaError_t e = launch_plan_device((const int32_t*)seq_lens->data, (int32_t)B, parts,
                                        plan->d_words, plan->layout, plan->d_err,
                                        (cudaStream_t)stream, 1);
