@@ -68,6 +68,22 @@ int32_t tc_min_q_len(bool fp8) {
   return v > 0 ? v : (fp8 ? 3 : 4);
 }
 
+// Parts of the tile plan hpc_decode_step builds for a step of this shape on
+// num_sms SMs: max(1, num_sms / H_kv) when q_len reaches the tensor-core
+// threshold (one CTA per (KV head, part)), else num_sms. Sets *tensor_core
+// accordingly.
+int32_t decode_plan_parts(const hpc_tensor* q, const hpc_tensor* k_cache, int32_t num_sms,
+                          bool* tensor_core) {
+  const int64_t T = (q && q->ndim == 4) ? q->shape[1] : 1;
+  const bool fp8 = k_cache && k_cache->dtype == HPC_FP8_E4M3;
+  const bool tc = q && q->ndim == 4 && T >= tc_min_q_len(fp8) && T <= kMaxQueryTokens;
+  if (tensor_core) *tensor_core = tc;
+  if (!tc) return num_sms;
+  const int64_t hkv =
+      (k_cache && k_cache->ndim == 4 && k_cache->shape[1] > 0) ? k_cache->shape[1] : 1;
+  return (int32_t)std::max<int64_t>(1, num_sms / hkv);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* ptr = nullptr;
@@ -228,17 +244,6 @@ hpc_status new_host_plan(const int32_t* words, const PlanLayout& L, int32_t kind
 
 void set_error(const std::string& msg) { g_last_error = msg; }
 
-int32_t decode_plan_parts(const hpc_tensor* q, const hpc_tensor* k_cache, int32_t num_sms,
-                          bool* tensor_core) {
-  const int64_t T = (q && q->ndim == 4) ? q->shape[1] : 1;
-  const bool fp8 = k_cache && k_cache->dtype == HPC_FP8_E4M3;
-  const bool tc = q && q->ndim == 4 && T >= tc_min_q_len(fp8) && T <= kMaxQueryTokens;
-  if (tensor_core) *tensor_core = tc;
-  if (!tc) return num_sms;
-  const int64_t hkv =
-      (k_cache && k_cache->ndim == 4 && k_cache->shape[1] > 0) ? k_cache->shape[1] : 1;
-  return (int32_t)std::max<int64_t>(1, num_sms / hkv);
-}
 
 }  // namespace hpc
 

@@ -191,13 +191,6 @@ cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_
 
 void set_error(const std::string& msg);
 
-// Parts of the tile plan hpc_decode_step builds for a step of this shape on
-// num_sms SMs:
-// max(1, num_sms / H_kv) when q_len reaches the tensor-core threshold (one
-// CTA per (KV head, part)), else num_sms. Sets *tensor_core accordingly.
-int32_t decode_plan_parts(const hpc_tensor* q, const hpc_tensor* k_cache, int32_t num_sms,
-                          bool* tensor_core);
-
 // Runs `set` (a cudaFuncSetAttribute call) once per device for one kernel:
 // kernel attributes belong to each device's copy of the function, so a
 // process that launches on several devices configures each of them. `done`
