@@ -166,3 +166,22 @@ def test_extend_argument_statuses(lib):
     assert status(a) == hpc.HPC_ERR_INVALID_ARG
     assert lib.hpc_extend_attn(None, None, None, None, None, None, None, None,
                                ctypes.c_float(-1.0), None, None) == hpc.HPC_ERR_INVALID_ARG
+
+
+def test_tensor_core_threshold_setting(lib):
+    # process-wide kernel choice for multi-token decode; no device involved
+    prev = hpc.hpc_decode_tc_min_q_len(-1)
+    try:
+        assert hpc.hpc_decode_tc_min_q_len(0) == prev      # 0: the per-dtype defaults
+        assert hpc.hpc_decode_tc_min_q_len(-1) == 0
+        assert hpc.hpc_decode_tc_min_q_len(6) == 0
+        assert hpc.hpc_decode_tc_min_q_len(-5) == 6         # negative: query only
+        assert hpc.hpc_decode_tc_min_q_len(9) == 6          # above 8: never
+        assert hpc.hpc_decode_tc_min_q_len(-1) == 9
+        with pytest.raises(hpc.HpcError) as ei:
+            hpc.hpc_decode_tc_min_q_len(1)
+        assert ei.value.status == hpc.HPC_ERR_INVALID_ARG
+        assert hpc.hpc_decode_tc_min_q_len(-1) == 9         # a refused call changes nothing
+        assert lib.hpc_decode_tc_min_q_len(-1, None) == hpc.HPC_OK  # previous may be NULL
+    finally:
+        hpc.hpc_decode_tc_min_q_len(prev)
