@@ -129,23 +129,29 @@ def test_tc_empty_sequences():
     assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
 
 
-def test_threshold_selects_the_tensor_core_kernel():
-    # the profiler's kernel list shows which kernel ran
-    w = W.make_workload(_cfg(64, 8), lengths=[700, 65], seed=80)
-    q = W.make_multi_query(w, 4, seed=81)
-
-    def kernels(threshold):
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            run(w, q, plan="step", threshold=threshold)
-        return " ".join(e.name for e in prof.events())
-
-    names = kernels(2)
-    if "kernel" not in names:
-        pytest.skip("the profiler recorded no CUDA kernels here")
-    assert "decode_tc_kernel" in names
-    names = kernels(9)
-    assert "decode_tc_kernel" not in names and "attn_kernel" in names
+def test_threshold_selects_the_tensor_core_plan():
+    # hpc_decode_step sizes its plan for the kernel it runs: num_sms / H_kv
+    # parts (one CTA per (KV head, part)) for the tensor-core kernel, num_sms
+    # for the one-warp-per-token kernel. Plan words: 3 = parts, 6 = the CTA
+    # count the plan was sized for.
+    w = W.make_workload(_cfg(64, 8), lengths=[12000, 65], seed=80)
+    q = W.make_multi_query(w, 4, seed=81).cuda()
+    d = device_workload(w)
+    sms = hpc.hpc_device_sm_count()
+    tiles = (12000 + 63) // 64 + (65 + 63) // 64
+    words = {}
+    for threshold in (2, 9):
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+        p = hpc.hpc_decode_plan_create(2, sms, 4 * 64)
+        with tc_threshold(threshold):
+            hpc.hpc_decode_step(q, d["k"], d["v"], d["bt"], d["sl"], p, sms, out, lse)
+            torch.cuda.synchronize()
+        assert hpc.hpc_decode_plan_status(p) == 0
+        words[threshold] = hpc.hpc_decode_plan_export(p)
+        p.destroy()
+    assert words[2][6] == sms // 8 and words[2][3] == min(sms // 8, tiles)
+    assert words[9][6] == sms and words[9][3] == min(sms, tiles)
 
 
 def test_threshold_argument_statuses():
