@@ -45,8 +45,8 @@ def _oracle(w, q):
                                      v_scale=w.v_scale)
 
 
-def run(w, q, plan="step", num_sms=None, threshold=2):
-    d = device_workload(w)
+def run(w, q, plan="step", num_sms=None, threshold=2, d=None):
+    d = d or device_workload(w)
     qd = q.to("cuda")
     B, T, hq = q.shape[0], q.shape[1], q.shape[2]
     sms = hpc.hpc_device_sm_count()
@@ -186,3 +186,67 @@ def test_tc_full_size_step_sampled(name, T):
     sub, qs = _subset(w, q, seqs)
     ref_out, ref_lse = _oracle(sub, qs)
     assert_parity(out[seqs], lse[seqs], ref_out, ref_lse, label=f"{name} q_len {T} sampled")
+
+
+def test_tc_block_permutation_gives_bit_identical_output():
+    # the block table is the only link between positions and physical blocks
+    w = W.make_workload(_cfg(64, 8, True), lengths=[700, 64, 3001, 129, 5], seed=83,
+                        slack_blocks=5)
+    q = W.make_multi_query(w, 4, seed=84)
+    out1, lse1 = run(w, q, plan="host", num_sms=19)
+    nb = w.k_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(85))
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt2 = w.block_table.clone()
+    m = bt2 >= 0
+    bt2[m] = perm[bt2[m].long()].to(torch.int32)
+    w.k_cache, w.v_cache, w.block_table = k2, v2, bt2
+    out2, lse2 = run(w, q, plan="host", num_sms=19)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_tc_permuted_view_cache_layout(fp8):
+    # a [blocks][64][H_kv][128] cache passed as a [blocks][H_kv][64][128] view
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=[300, 64, 1000], seed=86)
+    q = W.make_multi_query(w, 8, seed=87)
+    ref = run(w, q)
+    d = device_workload(w)
+    kt = d["k"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    vt = d["v"].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    assert kt.stride(1) == 128 and kt.stride(2) == 8 * 128
+    d["k"], d["v"] = kt, vt
+    got = run(w, q, d=d)
+    assert np.array_equal(ref[0], got[0]) and np.array_equal(ref[1], got[1])
+
+
+def test_tc_cuda_graph_capture_of_a_step():
+    # planner kernel, tensor-core kernel and merge captured once, replayed
+    sms = hpc.hpc_device_sm_count()
+    w = W.make_workload(_cfg(64, 8), lengths=[2000, 64, 700], seed=88)
+    q = W.make_multi_query(w, 4, seed=89)
+    d = device_workload(w)
+    qd = q.cuda()
+    out = torch.zeros(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(q.shape[:3], dtype=torch.float32, device="cuda")
+    p = hpc.hpc_decode_plan_create(3, sms, 4 * 64)
+    s = torch.cuda.Stream()
+    with tc_threshold(2):
+        with torch.cuda.stream(s):  # first call outside the capture
+            hpc.hpc_decode_step(qd, d["k"], d["v"], d["bt"], d["sl"], p, sms, out, lse, stream=s)
+        torch.cuda.synchronize()
+        out.zero_()
+        lse.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            hpc.hpc_decode_step(qd, d["k"], d["v"], d["bt"], d["sl"], p, sms, out, lse, stream=s)
+        g.replay()
+        torch.cuda.synchronize()
+    assert hpc.hpc_decode_plan_status(p) == 0
+    p.destroy()
+    ref_out, ref_lse = _oracle(w, q)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                  label="tc graph replay")
