@@ -257,7 +257,8 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
  * hpc_decode_step -- one whole decode step on the device: the balanced plan
  * of hpc_decode_plan_device, attention and merge, with the planning folded
  * into the attention kernel's start (each CTA derives its own part from the
- * device lengths), so a step is two kernel launches. Afterwards `plan` holds
+ * device lengths), so a step is two kernel launches (three on the
+ * tensor-core multi-token path below: planner kernel, attention, merge). Afterwards `plan` holds
  * this step's work list, word for word the host planner's for the same
  * lengths (hpc_decode_plan_compute_ex, hpc_decode_plan_export): a plan of
  * one unit per (tile, KV head) (units_per_tile = num_kv_heads) when
