@@ -281,14 +281,38 @@ def _subset(w, seqs):
                       w.softmax_scale, w.num_q_heads, w.num_kv_heads)
 
 
-def time_oracle(sample, reps):
+def time_oracle(sample, reps, keep=False):
+    """Wall times of `reps` oracle runs on the sample; with keep, also the
+    last run's (out, lse)."""
     import oracle
-    times = []
+    times, res = [], None
     for _ in range(reps):
         t0 = time.perf_counter()
-        oracle.decode_workload(sample)
+        res = oracle.decode_workload(sample)
         times.append(time.perf_counter() - t0)
-    return times
+    return (times, res) if keep else times
+
+
+def parity_summary(out, lse, ref_out, ref_lse, atol=1e-2, rtol=1e-2, lse_atol=1e-3):
+    """Worst errors of a GPU result against the oracle's for the same rows:
+    max |out - ref|, the largest ratio of that error to the bound
+    atol + rtol |ref| (<= 1 passes), max |lse - ref| over finite entries, and
+    whether the infinite lse entries (empty sequences) agree."""
+    import numpy as np
+    out, lse = np.asarray(out, dtype=np.float64), np.asarray(lse, dtype=np.float64)
+    ref_out, ref_lse = np.asarray(ref_out, dtype=np.float64), np.asarray(ref_lse, dtype=np.float64)
+    err = np.abs(out - ref_out)
+    ratio = err / (atol + rtol * np.abs(ref_out))
+    fin = np.isfinite(ref_lse)
+    lse_err = np.abs(lse[fin] - ref_lse[fin])
+    inf_match = bool(np.array_equal(np.isfinite(lse), fin))
+    worst_ratio = float(ratio.max()) if ratio.size else 0.0
+    worst_lse = float(lse_err.max()) if lse_err.size else 0.0
+    return {"max_abs_out_err": float(err.max()) if err.size else 0.0,
+            "max_err_over_bound": round(worst_ratio, 6),
+            "max_abs_lse_err": worst_lse, "lse_inf_match": inf_match,
+            "bounds": f"|out - ref| <= {atol} + {rtol}|ref|, |lse - ref| <= {lse_atol}",
+            "pass": bool(worst_ratio <= 1.0 and worst_lse <= lse_atol and inf_match)}
 
 
 # ------------------------------------------------------------- reference arm
@@ -589,13 +613,23 @@ def run_hpc(args, ws, rank, local):
     if not args.no_cpu_baseline and ws == 1 and rank == 0:
         import oracle
         sample, seqs = oracle_sample(w, budget_s=6.0)
-        times = time_oracle(sample, 3)
+        times, ref = time_oracle(sample, 3, keep=True)
         t = statistics.median(times)
         line["cpu_baseline"] = {
             "value": round(sample.algorithmic_bytes() / t / 1e9, 4), "unit": "GB/s",
             "cores": oracle.num_cpus(), "kind": "oracle",
             "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
                       f"{int(w.seq_lens.sum())} KV tokens), median of 3 runs, {t:.2f} s"}
+        # the step's own output on the same sequences against the oracle's
+        try:
+            torch.cuda.synchronize()
+            idx = torch.tensor(seqs, dtype=torch.long, device=out.device)
+            line["parity_sample"] = dict(
+                parity_summary(out[idx].double().cpu().numpy(), lse[idx].double().cpu().numpy(),
+                               ref[0], ref[1]),
+                sequences=len(seqs))
+        except Exception as e:  # a report, never a reason to lose the line
+            line["parity_sample"] = {"error": f"{type(e).__name__}: {e}"[:200]}
 
     # ---- multi-token decode (q_len new tokens per sequence share one KV read)
     if args.q_lens:

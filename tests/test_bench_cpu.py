@@ -1,0 +1,59 @@
+"""Host-side pieces of bench.py (no GPU): the parity report it adds to its
+JSON line, comparing the step's output on the oracle's sample sequences with
+the oracle's."""
+import numpy as np
+
+import bench
+
+
+def _case(seed=0):
+    rng = np.random.default_rng(seed)
+    ref_out = rng.standard_normal((3, 8, 128))
+    ref_lse = rng.standard_normal((3, 8))
+    ref_lse[1] = -np.inf  # an empty sequence
+    return ref_out, ref_lse
+
+
+def test_identical_results_pass_with_zero_error():
+    ref_out, ref_lse = _case()
+    r = bench.parity_summary(ref_out.copy(), ref_lse.copy(), ref_out, ref_lse)
+    assert r["pass"] and r["max_abs_out_err"] == 0 and r["max_abs_lse_err"] == 0
+    assert r["lse_inf_match"]
+
+
+def test_error_at_and_beyond_the_bound():
+    ref_out, ref_lse = _case(1)
+    out = ref_out.copy()
+    j = np.unravel_index(np.argmax(np.abs(ref_out)), ref_out.shape)
+    bound = 1e-2 + 1e-2 * abs(ref_out[j])
+    out[j] += 0.999 * bound
+    assert bench.parity_summary(out, ref_lse, ref_out, ref_lse)["pass"]
+    out[j] = ref_out[j] + 1.01 * bound
+    r = bench.parity_summary(out, ref_lse, ref_out, ref_lse)
+    assert not r["pass"] and 1.0 < r["max_err_over_bound"] < 1.02
+
+
+def test_lse_error_and_infinities():
+    ref_out, ref_lse = _case(2)
+    lse = ref_lse.copy()
+    lse[0, 0] += 2e-3
+    r = bench.parity_summary(ref_out, lse, ref_out, ref_lse)
+    assert not r["pass"] and abs(r["max_abs_lse_err"] - 2e-3) < 1e-12
+    lse = ref_lse.copy()
+    lse[1, 3] = 0.0  # an empty sequence reported with a finite lse
+    r = bench.parity_summary(ref_out, lse, ref_out, ref_lse)
+    assert not r["pass"] and not r["lse_inf_match"]
+
+
+def test_time_oracle_keeps_the_last_result():
+    # the bench's CPU leg times the oracle and keeps its result for the report
+    from paged_gqa_decode_hpc_gb300 import workloads as W
+    import oracle
+    w = W.make_workload("tiny")
+    times, (out, lse) = bench.time_oracle(w, 2, keep=True)
+    assert len(times) == 2 and all(t > 0 for t in times)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert np.array_equal(out, ref_out) and np.array_equal(lse, ref_lse)
+    assert len(bench.time_oracle(w, 1)) == 1
+    r = bench.parity_summary(out, lse, ref_out, ref_lse)
+    assert r["pass"]
