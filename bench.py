@@ -120,10 +120,25 @@ def extend_flops(lens, qn, num_q_heads):
 
 
 def kernel_source_digest():
+    """Digest of the attention kernel's source: attn_kernel.cu and every file
+    it includes from the package's csrc/ or include/ directories,
+    transitively."""
+    dirs = [os.path.join(ROOT, "paged_gqa_decode_hpc_gb300", "csrc"), os.path.join(ROOT, "include")]
     h = hashlib.sha256()
-    for name in ("attn_kernel.cu", "hpc_internal.h"):
-        with open(os.path.join(ROOT, "paged_gqa_decode_hpc_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    seen, todo = set(), ["attn_kernel.cu"]
+    while todo:
+        name = todo.pop(0)
+        if name in seen:
+            continue
+        path = next((os.path.join(d, name) for d in dirs
+                     if os.path.exists(os.path.join(d, name))), None)
+        if path is None:
+            continue  # a system header
+        seen.add(name)
+        with open(path, "rb") as f:
+            data = f.read()
+        h.update(name.encode() + b"\0" + data)
+        todo += re.findall(r'^\s*#\s*include\s+"([^"]+)"', data.decode("utf-8", "replace"), re.M)
     return h.hexdigest()[:16]
 
 
@@ -620,8 +635,12 @@ def run_hpc(args, ws, rank, local):
             "cores": oracle.num_cpus(), "kind": "oracle",
             "sample": f"{len(seqs)} of {B} sequences ({int(sample.seq_lens.sum())} of "
                       f"{int(w.seq_lens.sum())} KV tokens), median of 3 runs, {t:.2f} s"}
-        # the step's own output on the same sequences against the oracle's
+        # the step's own output on the same sequences against the oracle's: one
+        # dynamic step right here, so the report covers hpc_decode_step whatever
+        # legs ran before it
         try:
+            hpc.hpc_decode_step(q, kc, vc, bt, sl, plan, num_sms, out, lse, stream=stream,
+                                k_scale=w.k_scale, v_scale=w.v_scale)
             torch.cuda.synchronize()
             idx = torch.tensor(seqs, dtype=torch.long, device=out.device)
             line["parity_sample"] = dict(

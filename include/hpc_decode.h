@@ -324,14 +324,22 @@ hpc_status hpc_decode_plan_set_timing_events(hpc_plan_t plan, void* ev_start, vo
  * message): num_seqs <= HPC_NOALLOC_MAX_SEQS, CTAs <= HPC_NOALLOC_MAX_CTAS,
  * num_q_heads <= HPC_NOALLOC_MAX_Q_HEADS.
  *
- *   q, k_cache, v_cache, block_table, seq_lens, out, lse: as hpc_decode_attn
+ *   q, out      bf16 [B][H_q][128]: one query token per sequence only (the
+ *               multi-token [B][q_len][H_q][128] form of hpc_decode_attn is
+ *               refused with HPC_ERR_INVALID_ARG: its partial states would
+ *               need q_len times the scratch)
+ *   k_cache, v_cache, block_table, seq_lens, lse: as hpc_decode_attn
  *               (seq_lens on the device; the plan is built from them here)
  *   num_sms     CTAs of the persistent grid; <= 0 uses the device's SM count
  *   device_error  device int32 receiving HPC_DEVCHK_* bits by atomic OR (the
  *               caller zeroes it), or NULL to discard them
- * The first call on each device looks up the array's device address for that
+ * Every argument check is made before anything is enqueued: a call that
+ * returns an error has launched nothing and left the array as it was. The
+ * first call on each device looks up the array's device address for that
  * device (cudaGetSymbolAddress) with the device current; make that first call
- * before any stream capture. Every call uses the same array and it keeps the
+ * before any stream capture. The lookup is repeated only when the device's
+ * context has been replaced (after cudaDeviceReset the module, and with it the
+ * array, may sit elsewhere). Every call uses the same array and it keeps the
  * last call's contents, so calls whose work overlaps on the GPU (other
  * streams, other threads) race with each other: order them on one stream.
  */

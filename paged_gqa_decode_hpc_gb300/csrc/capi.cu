@@ -494,7 +494,7 @@ bool make_decode_q_map(const hpc_tensor* q, CUtensorMap* map) {
 hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_tensor* v_cache,
                      const hpc_tensor* block_table, const hpc_tensor* seq_lens, hpc_plan_t plan,
                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale, void* stream,
-                     int32_t fused_num_sms) {
+                     int32_t fused_num_sms, bool check_only) {
   hpc_status st;
   // q/out are [B][H_q][128] (one query token per sequence) or
   // [B][q_len][H_q][128] (q_len new tokens; lse then [B][q_len][H_q]).
@@ -585,6 +585,7 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
   }
   if (fp8 && (!std::isfinite(k_cache->scale) || !std::isfinite(v_cache->scale)))
     return fail(HPC_ERR_INVALID_ARG, "FP8 scales must be finite");
+  if (check_only) return HPC_OK;
   if (B == 0) return HPC_OK;
   if (B > INT32_MAX || block_table->shape[1] > INT32_MAX || NB > INT32_MAX)
     return fail(HPC_ERR_INVALID_ARG, "sizes exceed int32");
@@ -730,6 +731,15 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
 
 
 }  // namespace
+
+hpc_status check_decode_args(const hpc_tensor* q, const hpc_tensor* k_cache,
+                             const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                             const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                             hpc_tensor* lse) {
+  return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, nullptr, 0,
+                   true);
+}
+
 }  // namespace hpc
 
 extern "C" {
@@ -739,7 +749,7 @@ hpc_status hpc_decode_attn_ex(const hpc_tensor* q, const hpc_tensor* k_cache,
                               const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
                               hpc_tensor* lse, float softmax_scale, void* stream) {
   return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, softmax_scale,
-                   stream, 0);
+                   stream, 0, false);
 }
 
 hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
@@ -775,7 +785,7 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
     plan->host_num_segs = -1;
     plan->units = 1;
     return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
-                     0);
+                     0, false);
   }
   // One unit per (tile, KV head) when the kernel's warp layout takes all KV
   // heads in one pass with one warp per (head, token): an 8x finer partition.
@@ -799,7 +809,7 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
     plan->host_num_segs = -1;
     plan->units = units;
     return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
-                     0);
+                     0, false);
   }
   plan->units = units;
   plan->num_seqs = (int32_t)B;
@@ -807,7 +817,7 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
   plan->host_num_parts = -1;
   plan->host_num_segs = -1;
   return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
-                   num_sms);
+                   num_sms, false);
 }
 
 hpc_status hpc_decode_tc_min_q_len(int32_t q_len, int32_t* previous) {

@@ -191,6 +191,13 @@ cudaError_t launch_merge(const MergeParams& p, int32_t num_kv_heads, cudaStream_
 
 void set_error(const std::string& msg);
 
+// Every argument check hpc_decode_attn makes, with no launch and no
+// allocation (capi.cu).
+hpc_status check_decode_args(const hpc_tensor* q, const hpc_tensor* k_cache,
+                             const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                             const hpc_tensor* seq_lens, hpc_plan_t plan, hpc_tensor* out,
+                             hpc_tensor* lse);
+
 // Runs `set` (a cudaFuncSetAttribute call) once per device for one kernel:
 // kernel attributes belong to each device's copy of the function, so a
 // process that launches on several devices configures each of them. `done`

@@ -46,6 +46,25 @@ __device__ __forceinline__ uint32_t to_e4m3x4(float4 v) {
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// x / s rounded to odd in fp32: the quotient truncated toward zero, with its
+// lowest mantissa bit set when the division was inexact (the FMA remainder of
+// a faithfully rounded quotient is exact). A value rounded to odd with 24
+// significant bits and then rounded to nearest-even at e4m3's 4 bits equals
+// the nearest-even e4m3 of the exact quotient (Boldo and Melquiond, "When
+// double rounding is odd", 2005: a p-bit odd rounding followed by a
+// nearest rounding to at most p - 2 bits is a single correct rounding).
+__device__ __forceinline__ float div_round_odd(float x, float s) {
+  const float q = __fdiv_rz(x, s);
+  const float r = fmaf(-q, s, x);
+  return r != 0.f ? __uint_as_float(__float_as_uint(q) | 1u) : q;
+}
+
+// e4m3(v / s) of four values, each correctly rounded from the exact quotient.
+__device__ __forceinline__ uint32_t quantise_e4m3x4(float4 v, float s) {
+  return to_e4m3x4(make_float4(div_round_odd(v.x, s), div_round_odd(v.y, s),
+                               div_round_odd(v.z, s), div_round_odd(v.w, s)));
+}
+
 __global__ void __launch_bounds__(kRowsPerCta * 32) prologue_kernel(const PrologueParams p) {
   griddep_wait();
   griddep_launch_dependents();
@@ -104,9 +123,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) prologue_kernel(const Prolog
     *reinterpret_cast<uint2*>(p.q_out + (int64_t)b * p.qo_sb + (int64_t)h * p.qo_sh + d0) =
         to_bf16x4(x);
     if (p.q_fp8) {
-      const float is = 1.0f / p.q_fp8_scale;
       *reinterpret_cast<uint32_t*>(p.q_fp8 + (int64_t)b * p.qf_sb + (int64_t)h * p.qf_sh + d0) =
-          to_e4m3x4(make_float4(x.x * is, x.y * is, x.z * is, x.w * is));
+          quantise_e4m3x4(x, p.q_fp8_scale);
     }
     return;
   }
@@ -125,9 +143,8 @@ __global__ void __launch_bounds__(kRowsPerCta * 32) prologue_kernel(const Prolog
                       (int64_t)(pos % kBlockTokens) * p.c_sslot + d0;
   void* cache = kind == 1 ? p.k_cache : p.v_cache;
   if (p.cache_fp8) {
-    const float is = 1.0f / (kind == 1 ? p.k_scale : p.v_scale);
     *reinterpret_cast<uint32_t*>((uint8_t*)cache + off) =
-        to_e4m3x4(make_float4(x.x * is, x.y * is, x.z * is, x.w * is));
+        quantise_e4m3x4(x, kind == 1 ? p.k_scale : p.v_scale);
   } else {
     *reinterpret_cast<uint2*>((__nv_bfloat16*)cache + off) = to_bf16x4(x);
   }

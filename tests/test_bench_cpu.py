@@ -57,3 +57,27 @@ def test_time_oracle_keeps_the_last_result():
     assert len(bench.time_oracle(w, 1)) == 1
     r = bench.parity_summary(out, lse, ref_out, ref_lse)
     assert r["pass"]
+
+
+def test_kernel_source_digest_follows_includes(tmp_path, monkeypatch):
+    """The digest that keys the committed ncu traffic figure covers the kernel
+    file and every local header it includes, transitively, not the kernel
+    file alone: editing an included helper invalidates the figure."""
+    csrc = tmp_path / "paged_gqa_decode_hpc_gb300" / "csrc"
+    inc = tmp_path / "include"
+    csrc.mkdir(parents=True)
+    inc.mkdir()
+    (csrc / "attn_kernel.cu").write_text('#include <cuda.h>\n#include "a.h"\nkernel\n')
+    (csrc / "a.h").write_text('#include "b.cuh"\n#include "api.h"\n')
+    (csrc / "b.cuh").write_text("helper v1\n")
+    (inc / "api.h").write_text("abi v1\n")
+    (csrc / "unrelated.cu").write_text("other v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.kernel_source_digest()
+    (csrc / "unrelated.cu").write_text("other v2\n")
+    assert bench.kernel_source_digest() == d0
+    (csrc / "b.cuh").write_text("helper v2\n")
+    d1 = bench.kernel_source_digest()
+    assert d1 != d0
+    (inc / "api.h").write_text("abi v2\n")
+    assert bench.kernel_source_digest() != d1

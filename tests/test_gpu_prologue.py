@@ -55,14 +55,35 @@ def _close(got, ref):
     assert np.all(np.abs(got - ref) <= OUT_ATOL + OUT_RTOL * np.abs(ref)), np.abs(got - ref).max()
 
 
-def _check_codes(got_bytes, ref_vals, scale):
-    """e4m3 bytes vs the oracle's encoding of ref/scale: >= 99% identical and
-    every code within one step (fp32 vs fp64 rounding at a code boundary)."""
-    ref_codes = np.array([PR.e4m3_encode(x / scale) for x in ref_vals.ravel()], dtype=np.int64)
+def _oracle_codes(ref_vals, scale):
+    return np.array([PR.e4m3_encode(x / scale) for x in ref_vals.ravel()], dtype=np.int64)
+
+
+def _check_codes_exact(got_bytes, ref_vals, scale):
+    """A pure quantisation of exact bf16 inputs (the V row): reading p5 fixes
+    every byte, e4m3(x / scale) rounded to nearest even from the exact
+    quotient, so the kernel's bytes must equal the oracle's."""
+    ref_codes = _oracle_codes(ref_vals, scale)
+    got = got_bytes.ravel().astype(np.int64)
+    bad = np.flatnonzero(got != ref_codes)
+    assert bad.size == 0, (f"{bad.size} of {got.size} e4m3 bytes differ, first at {bad[0]}: "
+                           f"got {got[bad[0]]:#04x}, oracle {ref_codes[bad[0]]:#04x}")
+
+
+def _check_codes_near(got_bytes, ref_vals, scale, label):
+    """e4m3 bytes of a value the kernel computes in fp32 (normed and rotated
+    q and k) vs the oracle's encoding of its fp64 value: the two values differ
+    by fp32 rounding, which moves a value across a code boundary only when it
+    lies within that rounding of the boundary. Every code is within one step,
+    and the mismatches are few (reported, asserted below 1 %)."""
+    ref_codes = _oracle_codes(ref_vals, scale)
     got = got_bytes.ravel().astype(np.int64)
     mag = lambda c: np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
     assert np.all(np.abs(mag(got) - mag(ref_codes)) <= 1)
-    assert np.mean(got == ref_codes) >= 0.99
+    n_bad = int(np.sum(got != ref_codes))
+    print(f"{label}: {n_bad} of {got.size} e4m3 codes one step from the oracle's")
+    assert n_bad <= got.size // 100
+    return n_bad
 
 
 @pytest.mark.parametrize("hq,hkv,base", [(64, 8, 1e4), (8, 1, 1e6), (32, 4, 5e5)])
@@ -96,9 +117,29 @@ def test_prologue_fp8_cache_and_fp8_query():
     q_ref, k_ref, v_ref, slots = _oracle(w, pin)
     for b, (blk, slot) in enumerate(slots):
         _close(_f64(q_out[b]), q_ref[b])
-        _check_codes(q8[b].numpy(), q_ref[b], 0.02)
-        _check_codes(kc[blk, :, slot].numpy(), k_ref[b], w.k_scale)
-        _check_codes(vc[blk, :, slot].numpy(), v_ref[b], w.v_scale)
+        _check_codes_near(q8[b].numpy(), q_ref[b], 0.02, f"q seq {b}")
+        _check_codes_near(kc[blk, :, slot].numpy(), k_ref[b], w.k_scale, f"k seq {b}")
+        _check_codes_exact(vc[blk, :, slot].numpy(), v_ref[b], w.v_scale)
+
+
+def test_prologue_fp8_v_bytes_exact_on_many_rows():
+    """V quantisation alone over 256 sequences x 8 heads x 128 values with a
+    scale that is not a power of two, so the quotient is almost never exact
+    and every rounding decision is exercised (sub-normal and saturating codes
+    included: the inputs span 2^-12 .. 2^10 times the scale)."""
+    lens = [1 + (37 * i) % 200 for i in range(256)]
+    w = W.make_workload(_cfg(64, 8, fp8=True), lengths=lens, seed=59)
+    pin = W.make_prologue_inputs(w, seed=60)
+    g = torch.Generator().manual_seed(61)
+    mag = torch.exp2(torch.empty(pin.v_in.shape).uniform_(-12.0, 10.0, generator=g))
+    sgn = torch.where(torch.rand(pin.v_in.shape, generator=g) < 0.5, -1.0, 1.0)
+    v_in = (mag * sgn * w.v_scale).to(torch.bfloat16)
+    v_in[0, 0, :4] = torch.tensor([0.0, -0.0, 448.0 * w.v_scale, -1e4 * w.v_scale])
+    pin.v_in = v_in
+    _, _, _, vc = _run(w, pin)
+    _, _, v_ref, slots = _oracle(w, pin)
+    for b, (blk, slot) in enumerate(slots):
+        _check_codes_exact(vc[blk, :, slot].numpy(), v_ref[b], w.v_scale)
 
 
 def test_prologue_in_place_query_and_bad_block():
