@@ -19,6 +19,28 @@ formula; this oracle takes the plainest reading:
     listed by part and, within a part, by sequence;
   * a segment is WHOLE when it covers every tile of its sequence.
 
+Step plan -- the work list of one decode step with one query token, as the
+step call runs it. The same partition rule is applied to finer units, ordered
+so that a part's range holds whole (sequence, KV head) pairs where it can:
+  * sequence b has n_b * H_kv units; unit u of the sequence is tile u % n_b
+    of KV head u // n_b (head-major: a pair's tiles are adjacent);
+  * units are flattened in sequence order; T = sum_b n_b * H_kv;
+  * the last W = floor(T / 8) units form a pool, S = T - W units are static;
+  * P = min(num_sms, S) static parts, part p owning units
+    [floor(p*S/P), floor((p+1)*S/P)) (the rule above, over S units);
+  * the pool is cut into chunks of C = max(8, ceil(W / (4 * num_sms))) units,
+    chunk j owning [S + j*C, min(S + (j+1)*C, T)); chunks are taken at run
+    time by whichever CTA asks first (the pages' scheduler is static; this
+    small dynamic pool absorbs the SMs' unequal streaming rates, which no
+    static work estimate sees);
+  * owners are the parts 0..P-1 followed by the chunks P..P+chunks-1; a piece
+    is the intersection of an owner's range with one pair's units;
+  * a pair held by one piece is WHOLE (its result is final); otherwise each
+    of its k pieces leaves a partial state in slot 2*o if the piece is its
+    owner o's first piece, else 2*o + 1 (then it is the owner's last piece:
+    a piece strictly inside an owner's range is a whole pair), and the k
+    states are merged.
+
 Static plan -- the even split-KV schedule the pages compare against (same
 section: "static split-KV"; the 24-ai.news page notes it assumes uniform
 lengths). The split count is not given on the pages; the reading used is
@@ -120,3 +142,68 @@ def static_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int,
     part_seg_off = list(range(len(segments) + 1))  # one segment per part
     return Plan(sum(n), len(segments), segments, part_seg_off,
                 _seq_offsets(segments, len(n)))
+
+
+POOL_DIV = 8          # the pool holds floor(T / POOL_DIV) units
+MIN_CHUNK_UNITS = 8   # smallest pool chunk
+CHUNKS_PER_SM = 4     # at most this many chunks per CTA of the grid
+
+
+class Piece(NamedTuple):
+    owner: int       # static part p < P, or P + chunk index
+    seq: int
+    head: int        # KV head
+    tile_begin: int
+    tile_end: int
+    whole: bool      # covers every tile of its (sequence, head) pair
+    slot: int        # partial-state slot; -1 for a whole pair
+
+
+class StepPlan(NamedTuple):
+    num_units: int      # T
+    static_units: int   # S
+    num_parts: int      # P
+    chunk_units: int    # C
+    num_chunks: int
+    owner_start: List[int]   # [P + chunks + 1] first unit of every owner, then T
+    pieces: List[Piece]      # by owner, then in unit order
+    pair_pieces: dict        # (seq, head) -> number of pieces (pairs with tiles only)
+
+
+def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int) -> StepPlan:
+    if num_sms <= 0 or num_kv_heads <= 0 or any(L < 0 for L in seq_lens):
+        raise ValueError("num_sms and num_kv_heads must be positive, lengths non-negative")
+    n = tile_counts(seq_lens)
+    H = num_kv_heads
+    T = sum(c * H for c in n)
+    W = T // POOL_DIV
+    S = T - W
+    P = min(num_sms, S)
+    C = max(MIN_CHUNK_UNITS, -(-W // (CHUNKS_PER_SM * num_sms)))
+    chunks = -(-W // C)
+    owner_start = [(p * S) // P for p in range(P)] + [S + j * C for j in range(chunks)] + [T]
+    # every unit: (sequence, head, tile), in the flattened order
+    units = []
+    for b, nb in enumerate(n):
+        for h in range(H):
+            for t in range(nb):
+                units.append((b, h, t))
+    assert len(units) == T
+    pieces: List[Piece] = []
+    for o in range(P + chunks):
+        lo, hi = owner_start[o], owner_start[o + 1]
+        own: List[List[int]] = []   # [seq, head, tile_begin, tile_end]
+        for x in range(lo, hi):
+            b, h, t = units[x]
+            if own and own[-1][0] == b and own[-1][1] == h:
+                own[-1][3] = t + 1
+            else:
+                own.append([b, h, t, t + 1])
+        for i, (b, h, tb, te) in enumerate(own):
+            whole = tb == 0 and te == n[b]
+            slot = -1 if whole else (2 * o if i == 0 else 2 * o + 1)
+            pieces.append(Piece(o, b, h, tb, te, whole, slot))
+    pair_pieces: dict = {}
+    for pc in pieces:
+        pair_pieces[(pc.seq, pc.head)] = pair_pieces.get((pc.seq, pc.head), 0) + 1
+    return StepPlan(T, S, P, C, chunks, owner_start, pieces, pair_pieces)
