@@ -79,6 +79,8 @@ typedef struct hpc_plan_s* hpc_plan_t;
 /* Plan kinds reported in word 1 of an exported plan. */
 #define HPC_PLAN_DYNAMIC 0
 #define HPC_PLAN_STATIC 1
+/* The work list a one-token hpc_decode_step ran (see hpc_decode_step). */
+#define HPC_PLAN_STEP 2
 
 /* Segment flag: the segment covers every tile of its sequence. */
 #define HPC_SEG_WHOLE 1

@@ -33,7 +33,7 @@ __all__ = [
 HPC_OK, HPC_ERR_INVALID_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_CUDA, HPC_ERR_OOM, \
     HPC_ERR_DEVICE_CHECK = range(6)
 HPC_BF16, HPC_FP8_E4M3, HPC_F32, HPC_I32 = range(4)
-HPC_PLAN_DYNAMIC, HPC_PLAN_STATIC = 0, 1
+HPC_PLAN_DYNAMIC, HPC_PLAN_STATIC, HPC_PLAN_STEP = 0, 1, 2
 HPC_SEG_WHOLE = 1
 HPC_DEVCHK_BAD_LENGTH, HPC_DEVCHK_BAD_BLOCK, HPC_DEVCHK_TABLE_TOO_SHORT, \
     HPC_DEVCHK_TIMEOUT, HPC_DEVCHK_CAPACITY = 1, 2, 4, 8, 16

@@ -45,14 +45,11 @@ unsigned long long wait_limit_ns() {
 // Failure-path test switch: with HPC_DECODE_TEST_WITHHOLD_COPIES=1 the
 // producers of the attention and extend kernels issue no copies, so every
 // consumer wait runs out (bounded by HPC_DECODE_WAIT_LIMIT_MS) and the call
-// must come back with HPC_DEVCHK_TIMEOUT and a usable context. Read once per
-// process.
+// must come back with HPC_DEVCHK_TIMEOUT and a usable context. Read at every
+// call, so a test can follow a failed step with a normal one on the same plan.
 bool withhold_copies() {
-  static const bool v = [] {
-    const char* s = std::getenv("HPC_DECODE_TEST_WITHHOLD_COPIES");
-    return s && s[0] == '1';
-  }();
-  return v;
+  const char* s = std::getenv("HPC_DECODE_TEST_WITHHOLD_COPIES");
+  return s && s[0] == '1';
 }
 
 // Smallest q_len (new tokens per sequence) that hpc_decode_attn* and
@@ -102,6 +99,7 @@ void free_plan(hpc_plan_s* pl) {
   if (pl->d_words) cudaFree(pl->d_words);
   if (pl->d_err) cudaFree(pl->d_err);
   if (pl->d_ws) cudaFree(pl->d_ws);
+  if (pl->d_step) cudaFree(pl->d_step);
   if (pl->h_pinned) cudaFreeHost(pl->h_pinned);
   if (pl->copy_done) cudaEventDestroy(pl->copy_done);
   delete pl;
@@ -127,10 +125,13 @@ hpc_status ensure_workspace(hpc_plan_s* pl, int64_t num_q_heads, bool may_alloca
     cudaFree(pl->d_ws);
     pl->d_ws = nullptr;
   }
-  const size_t floats = (size_t)std::max<int64_t>(pl->layout.cap_segs, 1) * num_q_heads *
-                        (kHeadDim + 2);
+  size_t floats = (size_t)std::max<int64_t>(pl->layout.cap_segs, 1) * num_q_heads *
+                  (kHeadDim + 2);
+  if (pl->d_step)  // a one-token step's partial states
+    floats = std::max(floats, (size_t)step_ws_floats(pl->layout.cap_parts));
   HPC_CUDA_TRY(cudaMalloc(&pl->d_ws, floats * sizeof(float)));
   pl->ws_heads = num_q_heads;
+  pl->ws_floats = (int64_t)floats;
   return HPC_OK;
 }
 
@@ -336,6 +337,12 @@ hpc_status hpc_decode_plan_create(int32_t max_seqs, int32_t num_sms, int32_t num
   };
   hpc_status st = alloc_plan_buffers(pl);
   if (st != HPC_OK) return cleanup(st);
+  pl->step_kv_heads = std::max(1, num_q_heads / kGroup);
+  {
+    const size_t sb = (size_t)step_words(num_sms, max_seqs, pl->step_kv_heads) * sizeof(int32_t);
+    if (cudaMalloc(&pl->d_step, sb) != cudaSuccess || cudaMemset(pl->d_step, 0, sb) != cudaSuccess)
+      return cleanup(fail(HPC_ERR_OOM, "step counters allocation failed"));
+  }
   st = ensure_workspace(pl, num_q_heads, true);
   if (st != HPC_OK) return cleanup(st);
   const size_t bytes = (size_t)pl->layout.words() * sizeof(int32_t);
@@ -406,6 +413,22 @@ hpc_status hpc_decode_plan_export(hpc_plan_t plan, int32_t* buf, int64_t cap, in
   HPC_CUDA_TRY(cudaDeviceSynchronize());
   HPC_CUDA_TRY(cudaMemcpy(w.data(), plan->d_words, w.size() * sizeof(int32_t),
                           cudaMemcpyDeviceToHost));
+  if (w[kMagic] == kPlanMagic && w[kKind] == HPC_PLAN_STEP) {
+    // header, then one record per owner (parts, then pool chunks):
+    // first unit, end unit, pieces, executions since the plan was created
+    const int64_t owners = (int64_t)w[kNumParts] + w[kNumSegs];
+    if (!plan->d_step || owners < 0 || owners > (1 + kStepChunksPerCta) * (int64_t)L.cap_parts)
+      return fail(HPC_ERR_DEVICE_CHECK, "plan buffer is inconsistent");
+    const int64_t n = kHeaderWords + 4 * owners;
+    *len = n;
+    if (cap == 0 && !buf) return HPC_OK;
+    if (!buf || cap < n) return fail(HPC_ERR_INVALID_ARG, "export buffer too small");
+    for (int i = 0; i < kHeaderWords; ++i) buf[i] = w[i];
+    if (owners > 0)
+      HPC_CUDA_TRY(cudaMemcpy(buf + kHeaderWords, plan->d_step + step_rec_off(),
+                              (size_t)(4 * owners) * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    return HPC_OK;
+  }
   return write_canonical(w.data(), L, buf, cap, len);
 }
 
@@ -494,7 +517,7 @@ bool make_decode_q_map(const hpc_tensor* q, CUtensorMap* map) {
 hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_tensor* v_cache,
                      const hpc_tensor* block_table, const hpc_tensor* seq_lens, hpc_plan_t plan,
                      hpc_tensor* out, hpc_tensor* lse, float softmax_scale, void* stream,
-                     int32_t fused_num_sms, bool check_only) {
+                     int32_t fused_num_sms, bool check_only, int32_t step_grid = 0) {
   hpc_status st;
   // q/out are [B][H_q][128] (one query token per sequence) or
   // [B][q_len][H_q][128] (q_len new tokens; lse then [B][q_len][H_q]).
@@ -605,6 +628,54 @@ hpc_status attn_impl(const hpc_tensor* q, const hpc_tensor* k_cache, const hpc_t
 
   const PlanLayout& L = plan->layout;
   cudaStream_t s = (cudaStream_t)stream;
+  if (step_grid > 0) {
+    // one-token step: planned, computed and merged by the step kernel alone
+    if (!plan->d_step || Hkv > plan->step_kv_heads || step_grid > L.cap_parts ||
+        B > L.cap_seqs || plan->ws_floats < step_ws_floats(step_grid))
+      return fail(HPC_ERR_INVALID_ARG, "plan is too small for this step");
+    if (NB == 0) return fail(HPC_ERR_INVALID_ARG, "k_cache has no blocks");
+    CUtensorMap tk, tv;
+    if ((st = make_kv_map(k_cache, fp8, swap, &tk)) != HPC_OK) return st;
+    if ((st = make_kv_map(v_cache, fp8, swap, &tv)) != HPC_OK) return st;
+    StepParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.q = (const __nv_bfloat16*)q->data;
+    sp.q_sb = q->stride[0];
+    sp.q_sh = q->stride[1];
+    sp.out = (__nv_bfloat16*)out->data;
+    sp.o_sb = out->stride[0];
+    sp.o_sh = out->stride[1];
+    sp.lse = has_lse ? (float*)lse->data : nullptr;
+    sp.l_sb = has_lse ? lse->stride[0] : 0;
+    sp.l_sh = has_lse ? lse->stride[1] : 0;
+    sp.block_table = (const int32_t*)block_table->data;
+    sp.bt_sb = block_table->stride[0];
+    sp.max_blocks = (int32_t)block_table->shape[1];
+    sp.seq_lens = (const int32_t*)seq_lens->data;
+    sp.num_seqs = (int32_t)B;
+    sp.num_q_heads = (int32_t)Hq;
+    sp.num_kv_heads = (int32_t)Hkv;
+    sp.num_blocks = (int32_t)NB;
+    sp.kv_swap = swap;
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)kHeadDim);
+    sp.score_scale_log2 = scale * 1.4426950408889634f * (fp8 ? k_cache->scale : 1.0f);
+    sp.v_scale = fp8 ? v_cache->scale : 1.0f;
+    sp.ws_part = plan->d_ws;
+    sp.pool = plan->d_step;
+    sp.rec = plan->d_step + step_rec_off();
+    sp.pair_cnt = plan->d_step + step_pair_off(L.cap_parts);
+    sp.words = plan->d_words;
+    sp.err = plan->d_err;
+    sp.timeout_ns = wait_limit_ns();
+    sp.withhold_copies = withhold_copies();
+    if (plan->ev_start) HPC_CUDA_TRY(cudaEventRecord(plan->ev_start, s));
+    cudaError_t ce = launch_step(sp, tk, tv, fp8, step_grid, s);
+    if (ce != cudaSuccess)
+      return fail(HPC_ERR_CUDA, std::string("step kernel launch: ") + cudaGetErrorString(ce));
+    if (plan->ev_mid) HPC_CUDA_TRY(cudaEventRecord(plan->ev_mid, s));
+    if (plan->ev_end) HPC_CUDA_TRY(cudaEventRecord(plan->ev_end, s));
+    return HPC_OK;
+  }
   if (gx > 0) {
     if (NB == 0) return fail(HPC_ERR_INVALID_ARG, "k_cache has no blocks");
     CUtensorMap tk, tv;
@@ -786,6 +857,17 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
     plan->units = 1;
     return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
                      0, false);
+  }
+  // One query token per sequence: the step kernel plans, computes and merges
+  // the step alone (step_kernel.cu).
+  if (q->ndim == 3 && B <= kStepMaxSeqs && plan->d_step) {
+    plan->units = 1;
+    plan->num_seqs = (int32_t)B;
+    plan->num_sms = num_sms;
+    plan->host_num_parts = -1;
+    plan->host_num_segs = -1;
+    return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
+                     0, false, num_sms);
   }
   // One unit per (tile, KV head) when the kernel's warp layout takes all KV
   // heads in one pass with one warp per (head, token): an 8x finer partition.

@@ -61,6 +61,12 @@ struct hpc_plan_s {
   float* d_ws = nullptr;         // partial workspace: o [cap_segs][H_q][128], m, l
   int64_t ws_heads = 0;          // H_q the workspace was sized for
   cudaEvent_t ev_start = nullptr, ev_mid = nullptr, ev_end = nullptr;  // optional timing
+  // One-token step path (step_kernel.cu): pool counters, per-owner records and
+  // per-(sequence, KV head) arrival counters, zeroed at creation and left at
+  // zero by every step; sized for step_kv_heads KV heads.
+  int32_t* d_step = nullptr;
+  int32_t step_kv_heads = 0;
+  int64_t ws_floats = 0;         // floats allocated at d_ws
 };
 
 namespace hpc {
@@ -111,6 +117,51 @@ struct MergeParams {
   const float* ws_m;
   const float* ws_l;
 };
+
+// Parameter block of the one-token step kernel (step_kernel.cu).
+struct StepParams {
+  const __nv_bfloat16* q;
+  int64_t q_sb, q_sh;
+  __nv_bfloat16* out;
+  int64_t o_sb, o_sh;
+  float* lse;                   // may be null
+  int64_t l_sb, l_sh;
+  const int32_t* block_table;
+  int64_t bt_sb;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  int32_t num_seqs, num_q_heads, num_kv_heads, num_blocks;
+  int32_t kv_swap;
+  float score_scale_log2;
+  float v_scale;
+  float* ws_part;               // [slots][9][32] float4: partial states of split pairs
+                                //   in the consumer lanes' layout (step_kernel.cu)
+  int32_t* pool;                // [2]: next pool chunk, CTAs done claiming
+  int32_t* rec;                 // [owners][4]: first unit, end unit, pieces, runs
+  int32_t* pair_cnt;            // [num_seqs * num_kv_heads] arrival counters
+  int32_t* words;               // plan header words
+  int32_t* err;
+  unsigned long long timeout_ns;
+  int32_t withhold_copies;
+};
+// Step plan constants (the oracle's step_plan uses the same values).
+constexpr int32_t kStepPoolDiv = 8;      // pool = floor(T / 8) units
+constexpr int32_t kStepMinChunk = 8;     // smallest pool chunk, units
+constexpr int32_t kStepChunksPerCta = 4; // at most this many chunks per CTA
+constexpr int32_t kStepMaxSeqs = 3072;   // prefix array in shared memory
+constexpr int32_t kStepMinPartDiv = 8;   // P = min(G, ceil(S / 8)) static parts
+// d_step layout (int32 words): pool[2] | records[5 * cap_parts][4] | pair counters
+inline int64_t step_rec_off() { return 2; }
+inline int64_t step_pair_off(int32_t cap_parts) { return 2 + 4LL * (1 + kStepChunksPerCta) * cap_parts; }
+inline int64_t step_words(int32_t cap_parts, int32_t cap_seqs, int32_t kv_heads) {
+  return step_pair_off(cap_parts) + (int64_t)cap_seqs * kv_heads;
+}
+// Partial slots of a step on G CTAs: two per owner, owners <= G + 4 G; each
+// slot holds 9 x 32 float4 (8 accumulator slices and (m, l) per lane).
+inline int64_t step_slots(int32_t grid) { return 2LL * (1 + kStepChunksPerCta) * grid; }
+inline int64_t step_ws_floats(int32_t grid) { return step_slots(grid) * 9 * 32 * 4; }
+cudaError_t launch_step(const StepParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                        bool fp8, int grid, cudaStream_t stream);
 
 // Parameter block of the fused prologue kernel (prologue_kernel.cu).
 struct PrologueParams {

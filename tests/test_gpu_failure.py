@@ -27,15 +27,17 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 CHILD = r"""
-import json, sys, time
+import json, os, sys, time
 sys.path.insert(0, sys.argv[1])
+import numpy as np
 import torch
+import oracle
 import paged_gqa_decode_hpc_gb300 as hpc
 from paged_gqa_decode_hpc_gb300 import workloads as W
-from tests.gpu_util import device_workload
+from tests.gpu_util import assert_parity, device_workload
 hpc.load_library()
 res = {}
-for hkv, hq in ((8, 64), (1, 8)):  # without and with the warps' combine step
+for hkv, hq in ((8, 64), (1, 8)):  # one-token steps: the step kernel
     w = W.make_workload(W.Config(99, "fail", hq, hkv, "bf16"), lengths=[3000, 64, 700], seed=71)
     d = device_workload(w)
     sms = hpc.hpc_device_sm_count()
@@ -46,6 +48,16 @@ for hkv, hq in ((8, 64), (1, 8)):  # without and with the warps' combine step
     hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out)
     bits = hpc.hpc_decode_plan_status(plan)  # synchronises
     res[str(hkv)] = {"bits": bits, "seconds": time.time() - t0}
+    # the failed step left the plan's arrival counters and pool at zero: a
+    # normal step on the same plan is right
+    os.environ["HPC_DECODE_TEST_WITHHOLD_COPIES"] = "0"
+    lse = torch.zeros(w.q.shape[:2], dtype=torch.float32, device="cuda")
+    hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out, lse)
+    ok_bits = hpc.hpc_decode_plan_status(plan)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse)
+    res[str(hkv)]["recovered"] = ok_bits == 0
+    os.environ["HPC_DECODE_TEST_WITHHOLD_COPIES"] = "1"
     plan.destroy()
 # the tensor-core multi-token decode kernel (q_len 4), BF16 and FP8 caches
 for kvd in ("bf16", "fp8_e4m3"):
@@ -101,6 +113,7 @@ def test_withheld_copies_end_in_a_timeout_status_and_a_usable_context():
                 "extend_fp8_e4m3_1", "extend_fp8_e4m3_2"):
         assert res[key]["bits"] & hpc.HPC_DEVCHK_TIMEOUT, res
         assert res[key]["seconds"] < 30, res
+    assert res["8"]["recovered"] and res["1"]["recovered"], res
     assert res["usable"]
     # and this process, without the switch, still computes the right answer
     w = W.make_workload(W.Config(99, "fail", 64, 8, "bf16"), lengths=[3000, 64, 700], seed=71)

@@ -1,11 +1,16 @@
-"""hpc_decode_step: the attention kernel plans the step itself. Its output
-must match the oracle, equal the planner-kernel path bit for bit, and leave
-the same plan words as the planners."""
+"""hpc_decode_step: the kernels plan the step themselves. With one query token
+per sequence the step kernel runs alone (head-major units, static parts plus a
+pool of chunks, in-kernel merges of split pairs): its output must match the
+oracle, repeat bit for bit although pool chunks go to whichever CTA asks first,
+and its per-owner records must equal the oracle's step plan. Batches above the
+in-kernel limit run the planner kernel, the attention kernel and the merge,
+whose plan words equal the host planner's."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+from oracle import plan_ref
 import paged_gqa_decode_hpc_gb300 as hpc
 from paged_gqa_decode_hpc_gb300 import workloads as W
 from tests.gpu_util import assert_parity, device_workload, run_cuda
@@ -22,17 +27,6 @@ def _lib():
 
 def _cfg(hq=64, hkv=8, fp8=False):
     return W.Config(92, "step", hq, hkv, "fp8_e4m3" if fp8 else "bf16")
-
-
-def step_units(hkv, q_len=1, nc=8):
-    """Units per tile the step chooses: H_kv when one pass of one warp per
-    (head, token) covers all KV heads, else 1 (mirrors the library's rule)."""
-    hpass = max(1, nc // q_len)
-    hpass = min(hpass, hkv)
-    while hkv % hpass:
-        hpass -= 1
-    npass, tph = hkv // hpass, (nc // hpass) // q_len
-    return hkv if hkv > 1 and npass == 1 and tph == 1 else 1
 
 
 def run_plan_ex(w, units, num_sms):
@@ -68,6 +62,26 @@ def run_step(w, d=None, num_sms=None, plan=None):
     return out.double().cpu().numpy(), lse.double().cpu().numpy(), words, err
 
 
+def check_step_records(words, lens, num_sms, hkv, runs=1):
+    """The step's exported work list against the oracle's step plan: header,
+    then per owner (static parts, then pool chunks) its unit range, its number
+    of pieces and how many times a CTA ran it since the plan was created."""
+    sp = plan_ref.step_plan(list(lens), num_sms, hkv)
+    assert words[1] == hpc.HPC_PLAN_STEP
+    assert list(words[2:8]) == [len(lens), sp.num_parts, sp.num_units, sp.num_chunks, num_sms,
+                                hkv]
+    rec = np.asarray(words[8:]).reshape(-1, 4)
+    owners = sp.num_parts + sp.num_chunks
+    assert rec.shape[0] == owners
+    pieces = np.zeros(owners, dtype=np.int64)
+    for pc in sp.pieces:
+        pieces[pc.owner] += 1
+    assert np.array_equal(rec[:, 0], sp.owner_start[:-1])
+    assert np.array_equal(rec[:, 1], sp.owner_start[1:])
+    assert np.array_equal(rec[:, 2], pieces)
+    assert np.all(rec[:, 3] == runs), "every part and every pool chunk runs exactly once per step"
+
+
 @pytest.mark.parametrize("lens,hq,hkv,fp8,sms", [
     ([37, 64, 200, 1000], 8, 1, False, None),
     ([37, 64, 200, 1000], 8, 1, False, 1),
@@ -75,18 +89,21 @@ def run_step(w, d=None, num_sms=None, plan=None):
     ([1, 63, 64, 65, 127, 129, 700, 3001], 64, 8, True, None),
     ([0, 5, 0, 300, 4096, 0], 16, 2, False, 3),
     ([700, 65, 3001], 128, 16, False, None),
+    ([9000, 1, 2, 130], 32, 4, True, 2),
+    ([64] * 40 + [6400], 64, 8, False, 37),
 ])
-def test_step_parity_and_plan_words(lens, hq, hkv, fp8, sms):
+def test_step_parity_and_plan_records(lens, hq, hkv, fp8, sms):
     w = W.make_workload(_cfg(hq, hkv, fp8), lengths=lens, seed=41)
     ref_out, ref_lse = oracle.decode_workload(w)
     out, lse, words, err = run_step(w, num_sms=sms)
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label=f"step {lens[:4]}")
     n = sms or hpc.hpc_device_sm_count()
-    u = step_units(hkv)
-    assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(lens, n, u))
-    # a host plan with the same units gives the same bits
-    out2, lse2 = run_plan_ex(w, u, n)
+    check_step_records(words, lens, n, hkv)
+    # pool chunks go to whichever CTA asks first, yet every piece's arithmetic
+    # is fixed, so a second step gives the same bits
+    out2, lse2, _, err2 = run_step(w, num_sms=sms)
+    assert err2 == 0
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
@@ -96,8 +113,41 @@ def test_step_skewed_config():
     out, lse, words, err = run_step(w)
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label="step skewed")
-    assert np.array_equal(words, hpc.hpc_decode_plan_compute_ex(w.seq_lens.tolist(),
-                                                                 hpc.hpc_device_sm_count(), 8))
+    check_step_records(words, w.seq_lens.tolist(), hpc.hpc_device_sm_count(), 8)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_step_bit_identical_under_block_permutation(fp8):
+    """The same logical cache stored under another permutation of physical
+    blocks gives the same bits (the step reads tiles only through the table)."""
+    lens = [3000, 65, 1, 640, 129]
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=lens, seed=52)
+    out, lse, _, err = run_step(w, num_sms=19)
+    assert err == 0
+    nb = w.k_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(53))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nb)
+    bt2 = torch.where(w.block_table >= 0, inv[w.block_table.clamp(min=0).long()],
+                      w.block_table.long()).to(torch.int32)
+    w2 = W.Workload(w.config_name, w.seq_lens, bt2,
+                    w.q, w.k_cache[perm], w.v_cache[perm], w.k_scale, w.v_scale, w.kv_dtype,
+                    w.softmax_scale, w.num_q_heads, w.num_kv_heads)
+    out2, lse2, _, err2 = run_step(w2, num_sms=19)
+    assert err2 == 0
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_step_records_count_every_run():
+    lens = [4096] * 6 + [70]
+    w = W.make_workload(_cfg(64, 8), lengths=lens, seed=54)
+    d = device_workload(w)
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(len(lens), sms, 64)
+    for _ in range(3):
+        run_step(w, d=d, plan=plan)
+    check_step_records(hpc.hpc_decode_plan_export(plan), lens, sms, 8, runs=3)
+    plan.destroy()
 
 
 def test_step_many_sequences_uses_the_planner_kernel():

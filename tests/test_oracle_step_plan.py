@@ -32,8 +32,10 @@ def check_step(lengths, num_sms, H, sp):
     W = T - sp.static_units
     assert 0 <= W and 8 * W <= T < 8 * (W + 1)          # the pool is floor(T / 8)
     S, P, C = sp.static_units, sp.num_parts, sp.chunk_units
-    assert P == min(num_sms, S)
+    assert P == min(num_sms, -(-S // 8))   # at most one unit per consumer warp unless all SMs are used
     assert C >= 8 and sp.num_chunks * C >= W > (sp.num_chunks - 1) * C
+    if P:
+        assert 8 * P * C >= S            # a chunk is at least an eighth of a part
     assert sp.num_chunks <= 4 * num_sms
     # independent unit index of (b, h, t): sequences in order, then head, then tile
     cu = [0]
@@ -67,6 +69,7 @@ def check_step(lengths, num_sms, H, sp):
     if P:
         st = sizes[:P]
         assert sum(st) == S and max(st) - min(st) <= 1
+        assert P == num_sms or max(st) <= 8
         for (b, h, t), o in seen.items():
             x = uidx(b, h, t)
             if x < S:
