@@ -26,10 +26,15 @@ so that a part's range holds whole (sequence, KV head) pairs where it can:
     of KV head u // n_b (head-major: a pair's tiles are adjacent);
   * units are flattened in sequence order; T = sum_b n_b * H_kv;
   * the last W = floor(T / 8) units form a pool, S = T - W units are static;
-  * P = min(num_sms, S) static parts, part p owning units
-    [floor(p*S/P), floor((p+1)*S/P)) (the rule above, over S units);
-  * the pool is cut into chunks of C = max(8, ceil(W / (4 * num_sms))) units,
-    chunk j owning [S + j*C, min(S + (j+1)*C, T)); chunks are taken at run
+  * P = min(num_sms, ceil(S / 8)) static parts: no more parts than it takes
+    to give each CTA's 8 consumer warps one unit (they take a part's units
+    round-robin, and more, smaller parts would only cut pairs into more
+    pieces); part p owns units [floor(p*S/P), floor((p+1)*S/P)) (the rule
+    above, over S units);
+  * the pool is cut into chunks of C = max(8, ceil(S / (8 P)),
+    ceil(W / (4 * num_sms))) units -- an eighth of a static part, at least a
+    unit per consumer warp, at most 4 chunks per CTA -- chunk j owning
+    [S + j*C, min(S + (j+1)*C, T)); chunks are taken at run
     time by whichever CTA asks first (the pages' scheduler is static; this
     small dynamic pool absorbs the SMs' unequal streaming rates, which no
     static work estimate sees);
@@ -147,6 +152,7 @@ def static_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int,
 POOL_DIV = 8          # the pool holds floor(T / POOL_DIV) units
 MIN_CHUNK_UNITS = 8   # smallest pool chunk
 CHUNKS_PER_SM = 4     # at most this many chunks per CTA of the grid
+MIN_PART_UNITS = 8    # parts per 8 static units at most (one unit per consumer warp)
 
 
 class Piece(NamedTuple):
@@ -178,8 +184,8 @@ def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int) -> StepPlan:
     T = sum(c * H for c in n)
     W = T // POOL_DIV
     S = T - W
-    P = min(num_sms, S)
-    C = max(MIN_CHUNK_UNITS, -(-W // (CHUNKS_PER_SM * num_sms)))
+    P = min(num_sms, -(-S // MIN_PART_UNITS))
+    C = max(MIN_CHUNK_UNITS, -(-S // (8 * P)) if P else 0, -(-W // (CHUNKS_PER_SM * num_sms)))
     chunks = -(-W // C)
     owner_start = [(p * S) // P for p in range(P)] + [S + j * C for j in range(chunks)] + [T]
     # every unit: (sequence, head, tile), in the flattened order
