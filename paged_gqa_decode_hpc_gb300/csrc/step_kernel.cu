@@ -46,12 +46,22 @@ namespace hpc {
 namespace {
 
 constexpr int kSNC = 8;                           // consumer warps
-constexpr int kProducerWarp = kSNC, kEpilogueWarp = kSNC + 1;
-constexpr int kSThreads = (kSNC + 2) * 32;
+constexpr int kEpilogueWarps = 1;                 // epilogue warps, taking pieces in turn
+constexpr int kProducerWarp = kSNC, kEpilogueWarp0 = kSNC + 1;
+constexpr int kSThreads = (kSNC + 1 + kEpilogueWarps) * 32;
 constexpr int kPieceQ = 4;                        // piece descriptors in flight
+// A queue slot always serves the same epilogue warp, so the epilogue warps'
+// waits on descriptors are exact like the consumers'.
+static_assert(kPieceQ % kEpilogueWarps == 0, "queue slots per epilogue warp");
 constexpr int kDescInts = 8;
-constexpr int kDepSlices = kSNC + 1;              // 8 accumulator slices + (m, l)
-constexpr int kDepBytes = kSNC * kDepSlices * 32 * 16;  // one state per consumer warp
+// A consumer warp's deposit, per lane: its normalised output o = acc / l at
+// its 32 positions as 16-bit pairs (4 x 16 bytes) and (m, m, l, l) in fp32.
+// With an e4m3 cache |o| <= 448 and the pairs are fp16 (2^-11 rounding); with
+// a bf16 cache |o| is bounded only by the cache's values and the pairs are
+// bf16, whose range is fp32's. The accumulation itself stays fp32 throughout.
+constexpr int kDepSlices = kSNC + 1;              // 8 accumulator slices + (m, l) (partials)
+constexpr int kDepVec = 5;                        // 16-byte words per lane in a deposit
+constexpr int kDepBytes = kSNC * kDepVec * 32 * 16;  // one state per consumer warp
 // Waits on the descriptor queue and the deposits give up only this many data
 // waits later: once a data wait has timed out every role runs on without
 // copies, and this bookkeeping must then still finish, so that the arrival
@@ -65,8 +75,9 @@ struct StepCfg {
   static constexpr int kTile = Geom<FP8>::kTileBytes;
   static constexpr int kStage = Geom<FP8>::kStageBytes;
   static constexpr int kDepOff = STAGES * kStage;
-  // full, empty, piece full, piece free, deposit full, deposit free
-  static constexpr int kNumBars = 2 * STAGES + 2 * kPieceQ + 2;
+  // full, empty, piece full, piece free, deposit full (one per epilogue
+  // warp), deposit free
+  static constexpr int kNumBars = 2 * STAGES + 2 * kPieceQ + kEpilogueWarps + 1;
   static constexpr int kBarOff = kDepOff + kDepBytes;
   static constexpr int kIssuedOff = kBarOff + 8 * kNumBars;
   static constexpr int kDescOff = kIssuedOff + ((4 * STAGES + 15) / 16) * 16;
@@ -75,6 +86,25 @@ struct StepCfg {
   static constexpr int kSmemBytes = 1024 /* alignment slack */ + kPlanOff;
   static constexpr int kSmemBytesMax = kSmemBytes + 4 * (kStepMaxSeqs + 1);
 };
+
+// Orders this thread's earlier writes before its later ones at device scope
+// (release / acquire), lighter than a sequentially consistent fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack_dep(float lo, float hi) {
+  return FP8 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+template <bool FP8>
+__device__ __forceinline__ float2 unpack_dep(uint32_t v) {
+  if constexpr (FP8) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+  } else {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  }
+}
 
 // Owner arithmetic of the step plan: parts [0, P) over the first S units,
 // then chunks of C units up to T.
@@ -216,8 +246,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t bar_empty = bar_full + 8 * STAGES;
   const uint32_t bar_pfull = bar_empty + 8 * STAGES;
   const uint32_t bar_pfree = bar_pfull + 8 * kPieceQ;
-  const uint32_t bar_dfull = bar_pfree + 8 * kPieceQ;
-  const uint32_t bar_dfree = bar_dfull + 8;
+  const uint32_t bar_dfull = bar_pfree + 8 * kPieceQ;  // + 8 * (piece % kEpilogueWarps)
+  const uint32_t bar_dfree = bar_dfull + 8 * kEpilogueWarps;
   const uint32_t issued_word = smem_base + Cfg::kIssuedOff;
   int* desc = reinterpret_cast<int*>(smem + Cfg::kDescOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kMiscOff);
@@ -237,9 +267,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     for (int s = 0; s < kPieceQ; ++s) {
       mbar_init(bar_pfull + 8 * s, 1);
-      mbar_init(bar_pfree + 8 * s, kSNC + 1);  // consumer warps and the epilogue warp read it
+      mbar_init(bar_pfree + 8 * s, kSNC + 1);  // the consumer warps and the piece's epilogue warp
     }
-    mbar_init(bar_dfull, kSNC);  // every consumer warp has deposited its state of the piece
+    // every consumer warp has deposited its state of the piece; piece j on
+    // barrier j % kEpilogueWarps, so each barrier serves one epilogue warp
+    // and its phase k is that warp's k-th piece
+    for (int e = 0; e < kEpilogueWarps; ++e) mbar_init(bar_dfull + 8 * e, kSNC);
     mbar_init(bar_dfree, 1);     // the epilogue warp has read the deposits
     *abort_flag = 0;
     *s_bad = 0;
@@ -441,7 +474,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       p.pool[0] = 0;
       p.pool[1] = 0;
     }
-    publish(0, 0, 0, 0, kFlagEnd, -1);
+    // one end marker per epilogue warp (they take alternate pieces; the
+    // consumer warps stop at the first)
+    for (int e = 0; e < kEpilogueWarps; ++e) publish(0, 0, 0, 0, kFlagEnd, -1);
     named_bar_sync(3, kSThreads);
     if (lane == 0 && *abort_flag) {  // copies may still be landing: wait for the last ones
       for (uint32_t u = issued > (uint32_t)STAGES ? issued - STAGES : 0; u < issued; ++u)
@@ -452,7 +487,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 
   float4* dep = reinterpret_cast<float4*>(smem + Cfg::kDepOff);  // [warp][slice][lane]
-  if (warp == kEpilogueWarp) {
+  if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------ epilogue
     // For every piece: combine the consumer warps' 8 states (in warp order,
     // from shared memory), hand the deposit buffer back, then write the
@@ -461,7 +496,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // piece the merge of the pair. The global writes, fences and atomics of
     // this latency-heavy part never hold up the consumer warps.
     const int g8 = lane >> 2, c4 = lane & 3;
-    for (int j = 0;; ++j) {
+    for (int j = warp - kEpilogueWarp0;; j += kEpilogueWarps) {
       const int qs = j % kPieceQ;
       if (!wait_phase(bar_pfull + 8 * qs, (j / kPieceQ) & 1u, abort_flag, p.err, book_ns, false))
         break;
@@ -470,12 +505,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pfree + 8 * qs);
       if (fl & kFlagEnd) break;
-      if (!wait_phase(bar_dfull, j & 1u, abort_flag, p.err, book_ns, false)) break;
+      // the deposits of piece j complete phase j / kEpilogueWarps of this
+      // warp's barrier; its next phase needs this warp's read first, so the
+      // barrier is at most one phase ahead of the wait and the parity is exact
+      if (!wait_phase(bar_dfull + 8 * (j % kEpilogueWarps), (j / kEpilogueWarps) & 1u, abort_flag,
+                      p.err, book_ns, false))
+        break;
       // the 8 warps' states, combined in warp order
+      // acc = sum_v o_v l_v 2^(m_v - M): the unnormalised sum of the 8 states
+      const uint4* dep4 = reinterpret_cast<const uint4*>(dep);
       float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
       for (int v = 0; v < kSNC; ++v) {
-        const float2 mv = *reinterpret_cast<const float2*>(dep + (v * kDepSlices + 8) * 32 + lane);
+        const float2 mv =
+            *reinterpret_cast<const float2*>(dep4 + (v * kDepVec + 4) * 32 + lane);
         M0 = fmaxf(M0, mv.x);
         M1 = fmaxf(M1, mv.y);
       }
@@ -483,18 +526,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
       float acc[8][4];
 #pragma unroll
       for (int dm = 0; dm < 8; ++dm) acc[dm][0] = acc[dm][1] = acc[dm][2] = acc[dm][3] = 0.f;
-#pragma unroll
+      // a rolled loop: this code runs once per piece and often cold (its
+      // instructions fetched from DRAM), so it is kept short
+#pragma unroll 1
       for (int v = 0; v < kSNC; ++v) {
-        const float4 ml = dep[(v * kDepSlices + 8) * 32 + lane];
-        const float f0 = ml.x == -INFINITY ? 0.f : ex2(ml.x - M0);
-        const float f1 = ml.y == -INFINITY ? 0.f : ex2(ml.y - M1);
-        L0 += ml.z * f0;
-        L1 += ml.w * f1;
+        const float4 ml = *reinterpret_cast<const float4*>(dep4 + (v * kDepVec + 4) * 32 + lane);
+        const float w0 = ml.x == -INFINITY ? 0.f : ml.z * ex2(ml.x - M0);
+        const float w1 = ml.y == -INFINITY ? 0.f : ml.w * ex2(ml.y - M1);
+        L0 += w0;
+        L1 += w1;
 #pragma unroll
-        for (int dm = 0; dm < 8; ++dm) {
-          const float4 a4 = dep[(v * kDepSlices + dm) * 32 + lane];
-          acc[dm][0] += a4.x * f0; acc[dm][2] += a4.z * f0;
-          acc[dm][1] += a4.y * f1; acc[dm][3] += a4.w * f1;
+        for (int k = 0; k < 4; ++k) {
+          const uint4 h4 = dep4[(v * kDepVec + k) * 32 + lane];
+          const float2 a = unpack_dep<FP8>(h4.x), b2 = unpack_dep<FP8>(h4.y);
+          const float2 c2 = unpack_dep<FP8>(h4.z), d2 = unpack_dep<FP8>(h4.w);
+          acc[2 * k][0] += a.x * w0;  acc[2 * k][1] += a.y * w1;
+          acc[2 * k][2] += b2.x * w0; acc[2 * k][3] += b2.y * w1;
+          acc[2 * k + 1][0] += c2.x * w0; acc[2 * k + 1][1] += c2.y * w1;
+          acc[2 * k + 1][2] += d2.x * w0; acc[2 * k + 1][3] += d2.y * w1;
         }
       }
       __syncwarp();
@@ -523,7 +572,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         pd[dm * 32] = make_float4(acc[dm][0] * p.v_scale, acc[dm][1] * p.v_scale,
                                   acc[dm][2] * p.v_scale, acc[dm][3] * p.v_scale);
       pd[8 * 32] = make_float4(M0, M1, L0, L1);
-      __threadfence();  // this partial is visible device-wide before the pair is counted
+      fence_acq_rel_gpu();  // this partial is visible device-wide before the pair is counted
       __syncwarp();
       int last = 0;
       if (lane == 0) {
@@ -533,7 +582,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
-        __threadfence();
+        fence_acq_rel_gpu();  // acquire: every other piece's partial is visible
         merge_pair<FP8>(p, M, cu, b, h, lane);
       }
     }
@@ -599,13 +648,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     // deposit once the epilogue warp has read the previous piece's states
     wait_phase(bar_dfree, (j & 1u) ^ 1u, abort_flag, p.err, book_ns, false);
-    float4* dw = dep + (w * kDepSlices) * 32 + lane;
+    {
+      // approximate reciprocals: the result is rounded to 16 bits right after
+      const float i0 = l[0] > 0.f ? __fdividef(1.f, l[0]) : 0.f;
+      const float i1 = l[1] > 0.f ? __fdividef(1.f, l[1]) : 0.f;
+      uint4* dw = reinterpret_cast<uint4*>(dep) + (w * kDepVec) * 32 + lane;
 #pragma unroll
-    for (int dm = 0; dm < 8; ++dm)
-      dw[dm * 32] = make_float4(acc[dm][0], acc[dm][1], acc[dm][2], acc[dm][3]);
-    dw[8 * 32] = make_float4(m[0], m[1], l[0], l[1]);
+      for (int k = 0; k < 4; ++k)  // slices 2k, 2k + 1
+        dw[k * 32] = make_uint4(pack_dep<FP8>(acc[2 * k][0] * i0, acc[2 * k][1] * i1),
+                                pack_dep<FP8>(acc[2 * k][2] * i0, acc[2 * k][3] * i1),
+                                pack_dep<FP8>(acc[2 * k + 1][0] * i0, acc[2 * k + 1][1] * i1),
+                                pack_dep<FP8>(acc[2 * k + 1][2] * i0, acc[2 * k + 1][3] * i1));
+      reinterpret_cast<float4*>(dw)[4 * 32] = make_float4(m[0], m[1], l[0], l[1]);
+    }
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_dfull);  // release: the deposit is visible to the epilogue
+    if (lane == 0) mbar_arrive(bar_dfull + 8 * (j % kEpilogueWarps));  // release to the epilogue
   }
   named_bar_sync(3, kSThreads);  // see the producer's exit
 }
@@ -639,8 +696,8 @@ cudaError_t launch_step_cfg(const StepParams& p, const CUtensorMap& tk, const CU
 cudaError_t launch_step(const StepParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                         bool fp8, int grid, cudaStream_t stream) {
   if (p.num_seqs > kStepMaxSeqs) return cudaErrorInvalidValue;
-  return fp8 ? launch_step_cfg<true, 11>(p, tk, tv, grid, stream)
-             : launch_step_cfg<false, 5>(p, tk, tv, grid, stream);
+  return fp8 ? launch_step_cfg<true, 12>(p, tk, tv, grid, stream)
+             : launch_step_cfg<false, 6>(p, tk, tv, grid, stream);
 }
 
 }  // namespace hpc

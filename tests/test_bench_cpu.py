@@ -67,7 +67,7 @@ def test_kernel_source_digest_follows_includes(tmp_path, monkeypatch):
     inc = tmp_path / "include"
     csrc.mkdir(parents=True)
     inc.mkdir()
-    (csrc / "attn_kernel.cu").write_text('#include <cuda.h>\n#include "a.h"\nkernel\n')
+    (csrc / "step_kernel.cu").write_text('#include <cuda.h>\n#include "a.h"\nkernel\n')
     (csrc / "a.h").write_text('#include "b.cuh"\n#include "api.h"\n')
     (csrc / "b.cuh").write_text("helper v1\n")
     (inc / "api.h").write_text("abi v1\n")

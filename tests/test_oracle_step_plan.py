@@ -142,7 +142,8 @@ def test_pages_workload_shapes():
 def test_uniform_split_pairs_match_part_boundaries():
     """On the uniform batch the static parts (23 or 24 units) are longer than a
     pair (8 units), so each part boundary that falls strictly inside a pair
-    splits that pair in two, and no pair is cut twice."""
+    splits that pair in two and no pair is cut twice; the pool's 64 pairs
+    (sequences 56..63) are its 64 chunks, whole."""
     lens = [512] * 64
     sp = plan_ref.step_plan(lens, 152, 8)
     inside = sum(1 for p in range(1, 152) if (p * 3584 // 152) % 8 != 0)
