@@ -107,20 +107,26 @@ __device__ __forceinline__ float2 unpack_dep(uint32_t v) {
 }
 
 // Owner arithmetic of the step plan: parts [0, P) over the first S units,
-// then chunks of C units up to T.
+// then chunks of C units up to T. Every unit index is below T <= INT32_MAX,
+// so the arithmetic is 32-bit (short, fast code on a path that runs cold once
+// per step); the part formulas take 64 bits only when S * P does not fit.
 struct StepMath {
-  int64_t T, S, P, C, chunks;
-  PartMath pm;  // balanced parts over S units
-  __device__ __forceinline__ int64_t start(int64_t o) const {
-    return o < P ? pm.start(o) : S + (o - P) * C;
+  uint32_t T, S, P, C, chunks;
+  bool small;  // (S + 1) * (P + 1) < 2^32
+  __device__ __forceinline__ uint32_t part_start(uint32_t o) const {
+    return small ? o * S / P : (uint32_t)((uint64_t)o * S / P);
   }
-  __device__ __forceinline__ int64_t end(int64_t o) const {
-    if (o < P) return o + 1 < P ? pm.start(o + 1) : S;
-    const int64_t e = S + (o - P + 1) * C;
+  __device__ __forceinline__ uint32_t start(uint32_t o) const {
+    return o < P ? part_start(o) : S + (o - P) * C;
+  }
+  __device__ __forceinline__ uint32_t end(uint32_t o) const {
+    if (o < P) return o + 1 < P ? part_start(o + 1) : S;
+    const uint32_t e = S + (o - P + 1) * C;
     return e < T ? e : T;
   }
-  __device__ __forceinline__ int64_t owner_of(int64_t x) const {
-    return x < S ? pm.of(x) : P + (x - S) / C;
+  __device__ __forceinline__ uint32_t owner_of(uint32_t x) const {
+    if (x < S) return small ? ((x + 1) * P - 1) / S : (uint32_t)(((uint64_t)(x + 1) * P - 1) / S);
+    return P + (x - S) / C;
   }
 };
 
@@ -160,22 +166,22 @@ template <bool FP8>
 __device__ __forceinline__ void merge_pair(const StepParams& p, const StepMath& M,
                                            const int32_t* cu, int b, int h, int lane) {
   const int g = lane >> 2, c = lane & 3;
-  const int nb = (cu[b + 1] - cu[b]) / p.num_kv_heads;
-  const int64_t A = cu[b] + (int64_t)h * nb;
-  const int64_t first = M.owner_of(A), last = M.owner_of(A + nb - 1);
+  const uint32_t nb = (uint32_t)(cu[b + 1] - cu[b]) / (uint32_t)p.num_kv_heads;
+  const uint32_t A = (uint32_t)cu[b] + (uint32_t)h * nb;
+  const uint32_t first = M.owner_of(A), last = M.owner_of(A + nb - 1);
   const float4* part = reinterpret_cast<const float4*>(p.ws_part);
   float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
   float acc[8][4];
 #pragma unroll
   for (int dm = 0; dm < 8; ++dm) acc[dm][0] = acc[dm][1] = acc[dm][2] = acc[dm][3] = 0.f;
   constexpr int kBatch = 2;
-  for (int64_t o0 = first; o0 <= last; o0 += kBatch) {
+  for (uint32_t o0 = first; o0 <= last; o0 += kBatch) {
     float4 st[kBatch][kDepSlices];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
-      const int64_t ow = o0 + u;
+      const uint32_t ow = o0 + u;
       if (ow <= last) {
-        const int64_t s = 2 * ow + (A <= M.start(ow) ? 0 : 1);
+        const int64_t s = 2 * (int64_t)ow + (A <= M.start(ow) ? 0 : 1);
         const float4* src = part + s * kPartFloat4 + lane;
 #pragma unroll
         for (int k = 0; k < kDepSlices; ++k) st[u][k] = __ldcg(src + k * 32);
@@ -306,25 +312,22 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
   const bool bad = *s_bad != 0 || carry > INT32_MAX;
   StepMath M;
-  M.T = bad ? 0 : carry;
-  const int64_t W = M.T / kStepPoolDiv;
+  M.T = bad ? 0u : (uint32_t)carry;
+  const uint32_t W = M.T / kStepPoolDiv;
   M.S = M.T - W;
   {
-    const int64_t want = (M.S + kStepMinPartDiv - 1) / kStepMinPartDiv;  // one unit per consumer warp
-    M.P = want < G ? want : G;
-  }
-  {
+    const uint32_t want = (M.S + kStepMinPartDiv - 1) / kStepMinPartDiv;  // a unit per consumer warp
+    M.P = want < (uint32_t)G ? want : (uint32_t)G;
     // an eighth of a static part, at least one unit per consumer warp, at
     // most kStepChunksPerCta chunks per CTA
-    const int64_t per = (int64_t)kStepChunksPerCta * G;
-    int64_t c = (W + per - 1) / per;
-    const int64_t eighth = M.P > 0 ? (M.S + 8 * M.P - 1) / (8 * M.P) : 0;
+    const uint32_t per = (uint32_t)kStepChunksPerCta * (uint32_t)G;
+    uint32_t c = (W + per - 1) / per;
+    const uint32_t eighth = M.P > 0 ? (M.S + 8 * M.P - 1) / (8 * M.P) : 0;
     c = c > eighth ? c : eighth;
-    M.C = c > kStepMinChunk ? c : kStepMinChunk;
+    M.C = c > (uint32_t)kStepMinChunk ? c : (uint32_t)kStepMinChunk;
   }
   M.chunks = (W + M.C - 1) / M.C;
-  M.pm = PartMath{M.S, M.P, (M.S + 1) * (M.P + 1) < (int64_t)UINT32_MAX};
-
+  M.small = (uint64_t)(M.S + 1) * (M.P + 1) < (uint64_t)UINT32_MAX;
   if (blockIdx.x == 0 && tid == 0) {
     if (bad) atomicOr(p.err, HPC_DEVCHK_BAD_LENGTH);
     if (p.words) {
@@ -334,9 +337,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
   }
   // sequences without tiles (or a bad step): out = 0, lse = -inf
-  for (int64_t r = (int64_t)blockIdx.x * kSThreads + tid; r < (int64_t)B * p.num_q_heads;
-       r += (int64_t)G * kSThreads) {
-    const int b = (int)(r / p.num_q_heads), j = (int)(r % p.num_q_heads);
+  for (uint32_t r = blockIdx.x * kSThreads + tid; r < (uint32_t)B * (uint32_t)p.num_q_heads;
+       r += (uint32_t)G * kSThreads) {
+    const int b = (int)(r / (uint32_t)p.num_q_heads);
+    const int j = (int)(r - (uint32_t)b * (uint32_t)p.num_q_heads);
     if (bad || cu[b + 1] == cu[b]) {
       uint4* o = reinterpret_cast<uint4*>(p.out + (int64_t)b * p.o_sb + (int64_t)j * p.o_sh);
 #pragma unroll
@@ -360,10 +364,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       if (lane == 0) pend = atomicAdd(p.pool, 1);
       asked = true;
     };
-    auto resolve = [&]() -> int64_t {
+    auto resolve = [&]() -> int {
       const int c = __shfl_sync(0xffffffffu, pend, 0);
       asked = false;
-      return c < M.chunks ? M.P + c : -1;
+      return (uint32_t)c < M.chunks ? (int)(M.P + (uint32_t)c) : -1;
     };
     auto publish = [&](int b, int h, int t0, int t1, int flags, int slot) {
       if (lane == 0 && !lost) {
@@ -380,35 +384,36 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       ++j;
     };
-    int64_t owner;
-    if ((int64_t)blockIdx.x < M.P) {
+    int owner;
+    if (blockIdx.x < M.P) {
       owner = blockIdx.x;
     } else {
       ask();
       owner = resolve();
     }
     while (owner >= 0) {
-      const int64_t lo = M.start(owner), hi = M.end(owner);
+      const uint32_t lo = M.start(owner), hi = M.end(owner);
       int npieces = 0;
       int b;
       {
         int l0 = 0, h0 = B;  // last b with cu[b] <= lo
         while (h0 - l0 > 1) {
           const int mid = (l0 + h0) >> 1;
-          if (cu[mid] <= lo) l0 = mid; else h0 = mid;
+          if ((uint32_t)cu[mid] <= lo) l0 = mid; else h0 = mid;
         }
         b = l0;
       }
-      for (int64_t u = lo; u < hi;) {
-        while (cu[b + 1] <= u) ++b;
-        const int nb = (cu[b + 1] - cu[b]) / H;
-        const int64_t rel = u - cu[b];
-        const int h = (int)(rel / nb), t0 = (int)(rel % nb);
-        const int64_t pair_lo = cu[b] + (int64_t)h * nb, pair_hi = pair_lo + nb;
-        const int64_t e = hi < pair_hi ? hi : pair_hi;
+      for (uint32_t u = lo; u < hi;) {
+        while ((uint32_t)cu[b + 1] <= u) ++b;
+        const uint32_t nb = (uint32_t)(cu[b + 1] - cu[b]) / (uint32_t)H;
+        const uint32_t rel = u - (uint32_t)cu[b];
+        const uint32_t hu = rel / nb;
+        const int h = (int)hu, t0 = (int)(rel - hu * nb);
+        const uint32_t pair_lo = (uint32_t)cu[b] + hu * nb, pair_hi = pair_lo + nb;
+        const uint32_t e = hi < pair_hi ? hi : pair_hi;
         const int t1 = t0 + (int)(e - u);
-        const bool whole = t0 == 0 && t1 == nb;
-        const int slot = whole ? -1 : (int)(u == lo ? 2 * owner : 2 * owner + 1);
+        const bool whole = t0 == 0 && t1 == (int)nb;
+        const int slot = whole ? -1 : (u == lo ? 2 * owner : 2 * owner + 1);
         const int k = whole ? 1 : (int)(M.owner_of(pair_hi - 1) - M.owner_of(pair_lo) + 1);
         publish(b, h, t0, t1, (whole ? kFlagWhole : 0) | (k << 8), slot);
         ++npieces;
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
           const int cnt = n - i0 < 32 ? n - i0 : 32;
           for (int ii = 0; ii < cnt; ++ii, ++g) {
             const int bk = __shfl_sync(0xffffffffu, blk, ii);
-            if (!asked && hi - (u + i0 + ii) <= kClaimAhead) ask();
+            if (!asked && hi - (u + (uint32_t)(i0 + ii)) <= (uint32_t)kClaimAhead) ask();
             if (lane != 0 || stop) continue;
             const uint32_t slot_r = g % STAGES;
             if (!wait_phase(bar_empty + 8 * slot_r, ((g / STAGES) & 1u) ^ 1u, abort_flag, p.err,
