@@ -31,8 +31,8 @@ so that a part's range holds whole (sequence, KV head) pairs where it can:
     round-robin, and more, smaller parts would only cut pairs into more
     pieces); part p owns units [floor(p*S/P), floor((p+1)*S/P)) (the rule
     above, over S units);
-  * the pool is cut into chunks of C = max(8, ceil(S / (8 P)),
-    ceil(W / (4 * num_sms))) units -- an eighth of a static part, at least a
+  * the pool is cut into chunks of C = max(8, ceil(S / (12 P)),
+    ceil(W / (4 * num_sms))) units -- a twelfth of a static part, at least a
     unit per consumer warp, at most 4 chunks per CTA -- chunk j owning
     [S + j*C, min(S + (j+1)*C, T)); chunks are taken at run
     time by whichever CTA asks first (the pages' scheduler is static; this
@@ -153,6 +153,7 @@ POOL_DIV = 8          # the pool holds floor(T / POOL_DIV) units
 MIN_CHUNK_UNITS = 8   # smallest pool chunk
 CHUNKS_PER_SM = 4     # at most this many chunks per CTA of the grid
 MIN_PART_UNITS = 8    # parts per 8 static units at most (one unit per consumer warp)
+PART_CHUNKS = 12      # a pool chunk is at least this fraction (1/12) of a static part
 
 
 class Piece(NamedTuple):
@@ -185,7 +186,8 @@ def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int) -> StepPlan:
     W = T // POOL_DIV
     S = T - W
     P = min(num_sms, -(-S // MIN_PART_UNITS))
-    C = max(MIN_CHUNK_UNITS, -(-S // (8 * P)) if P else 0, -(-W // (CHUNKS_PER_SM * num_sms)))
+    C = max(MIN_CHUNK_UNITS, -(-S // (PART_CHUNKS * P)) if P else 0,
+            -(-W // (CHUNKS_PER_SM * num_sms)))
     chunks = -(-W // C)
     owner_start = [(p * S) // P for p in range(P)] + [S + j * C for j in range(chunks)] + [T]
     # every unit: (sequence, head, tile), in the flattened order

@@ -35,7 +35,7 @@ def check_step(lengths, num_sms, H, sp):
     assert P == min(num_sms, -(-S // 8))   # at most one unit per consumer warp unless all SMs are used
     assert C >= 8 and sp.num_chunks * C >= W > (sp.num_chunks - 1) * C
     if P:
-        assert 8 * P * C >= S            # a chunk is at least an eighth of a part
+        assert 12 * P * C >= S           # a chunk is at least a twelfth of a part
     assert sp.num_chunks <= 4 * num_sms
     # independent unit index of (b, h, t): sequences in order, then head, then tile
     cu = [0]
@@ -159,3 +159,17 @@ def test_empty_and_degenerate():
     assert sp.pieces[0].whole
     with pytest.raises(ValueError):
         plan_ref.step_plan([-1], 4, 1)
+
+
+def test_skewed_pool_chunks_are_quarter_pairs():
+    """On the skewed batch the pool (the last 4032 units) starts on a pair
+    boundary (S = 441 * 64) and a chunk is a twelfth of a part rounded up,
+    16 units: every pool chunk is one piece, a quarter of a 64-unit pair, and
+    each of those 63 pairs is merged from exactly 4 pieces."""
+    lens = [131072] + [4096] * 31
+    sp = plan_ref.step_plan(lens, 152, 8)
+    pool = [pc for pc in sp.pieces if pc.owner >= sp.num_parts]
+    assert len(pool) == sp.num_chunks == 252
+    assert all(pc.tile_end - pc.tile_begin == 16 and not pc.whole for pc in pool)
+    pairs = {(pc.seq, pc.head) for pc in pool}
+    assert len(pairs) == 63 and all(sp.pair_pieces[k] == 4 for k in pairs)
