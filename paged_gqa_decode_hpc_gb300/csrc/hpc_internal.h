@@ -150,6 +150,7 @@ constexpr int32_t kStepMinChunk = 8;     // smallest pool chunk, units
 constexpr int32_t kStepChunksPerCta = 4; // at most this many chunks per CTA
 constexpr int32_t kStepMaxSeqs = 3072;   // prefix array in shared memory
 constexpr int32_t kStepMinPartDiv = 8;   // P = min(G, ceil(S / 8)) static parts
+constexpr int32_t kStepPartChunks = 12;  // a pool chunk is at least 1/12 of a static part
 // d_step layout (int32 words): pool[2] | records[5 * cap_parts][4] | pair counters
 inline int64_t step_rec_off() { return 2; }
 inline int64_t step_pair_off(int32_t cap_parts) { return 2 + 4LL * (1 + kStepChunksPerCta) * cap_parts; }

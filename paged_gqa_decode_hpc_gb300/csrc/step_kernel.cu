@@ -318,12 +318,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   {
     const uint32_t want = (M.S + kStepMinPartDiv - 1) / kStepMinPartDiv;  // a unit per consumer warp
     M.P = want < (uint32_t)G ? want : (uint32_t)G;
-    // an eighth of a static part, at least one unit per consumer warp, at
+    // a twelfth of a static part, at least one unit per consumer warp, at
     // most kStepChunksPerCta chunks per CTA
     const uint32_t per = (uint32_t)kStepChunksPerCta * (uint32_t)G;
     uint32_t c = (W + per - 1) / per;
-    const uint32_t eighth = M.P > 0 ? (M.S + 8 * M.P - 1) / (8 * M.P) : 0;
-    c = c > eighth ? c : eighth;
+    const uint32_t frac = (uint32_t)kStepPartChunks * M.P;
+    const uint32_t twelfth = M.P > 0 ? (M.S + frac - 1) / frac : 0;
+    c = c > twelfth ? c : twelfth;
     M.C = c > (uint32_t)kStepMinChunk ? c : (uint32_t)kStepMinChunk;
   }
   M.chunks = (W + M.C - 1) / M.C;
