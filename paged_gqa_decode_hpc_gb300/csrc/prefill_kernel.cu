@@ -15,12 +15,18 @@
 // tile, so the work is a dense contraction and runs on tcgen05:
 //  * CTA = (KV head, QT tiles of 16 new tokens of one sequence), QT = 1 or 2.
 //    Warps: 4 softmax warps per query tile (thread = query row = TMEM lane),
-//    4 e4m3 -> bf16 converter warps (FP8 caches only), 1 TMA producer warp,
+//    4 e4m3 -> f16 converter warps (FP8 caches only), 1 TMA producer warp,
 //    1 MMA warp per query tile (the tiles' pipelines never wait on each other).
 //  * TMA loads Q once (3-D map over [token][head][128], box 16 x 8 x 64,
 //    128-byte swizzle: row t*8+g of the tile is query head g of token t) and
 //    the K / V tiles of the sequence's blocks into a shared-memory ring (for
-//    FP8, into an e4m3 ring that the converters widen into the bf16 ring).
+//    FP8, into an e4m3 ring that the converters widen into the 16-bit ring).
+//  * FP8 caches run the MMAs in fp16: every e4m3 value is an f16 value (one
+//    conversion per pair), each softmax thread converts its own Q row in
+//    place to f16 with a power-of-two scale putting the row's max |q| in
+//    [2^14, 2^15) (exact for every bf16 value that lands in f16's normal
+//    range) and takes the scale back out of its logit scale, and P is packed
+//    as f16 (P < 256). BF16 caches run everything in bf16.
 //  * S_j = Q K_j^T (M 128, N 64, K 128, both operands K-major in shared
 //    memory) into tensor memory; S is single-buffered and S_{j+1} is issued
 //    as soon as the softmax warps have copied S_j out.
@@ -29,7 +35,7 @@
 //    tensor memory) when a row's maximum grows by more than 8 (a factor 256):
 //    P = 2^(s - m) then stays below 256, and the final O / l uses one
 //    consistent m per row.
-//  * P (bf16 pairs) goes back to tensor memory (double-buffered) and
+//  * P (16-bit pairs) goes back to tensor memory (double-buffered) and
 //    O += P V_j (M 128, N 128, K 64) reads A = P from tensor memory and V as
 //    the MN-major operand of its tile; O accumulates in tensor memory.
 //  * Epilogue: O * v_scale / l -> bf16 rows of out, lse = ln 2 (m + log2 l).
@@ -81,8 +87,8 @@ struct Layout {
   static constexpr uint32_t kOffKV8 = kOffKV + kStages * kStageBytes;    // stages8 x 16 KB
   static constexpr uint32_t kOffBar = kOffKV8 + kStages8 * kStageBytes8;
   // q_full, kv_full[S], kv_empty[S], kv8_full[S8], kv8_empty[S8],
-  // per tile: s_full, s_free, p_full[2], pv_done[2], drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kStages8 + 7 * QT;
+  // per tile: s_full, s_free, p_full[2], pv_done[2], drain, q_ready (FP8)
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * kStages8 + 8 * QT;
   static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align to 1024
   // tensor memory per query tile: S (64 columns) | P0, P1 (32 each, bf16 pairs) | O (128)
@@ -125,14 +131,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
-// Two e4m3 bytes (low byte -> low half) to bf16x2, exactly: e4m3 -> f16 is
-// exact, and every e4m3 value is a bf16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t x) {
+// Two e4m3 bytes (low byte -> low half) to f16x2, exactly: every e4m3 value
+// is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(x));
-  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
-  return pack_bf16(lo, hi);
+  return h;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -269,12 +278,13 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
   auto kv_empty = [&](int s) { return bars + 8u * (1 + S + s); };
   auto kv8_full = [&](int s) { return bars + 8u * (1 + 2 * S + s); };
   auto kv8_empty = [&](int s) { return bars + 8u * (1 + 2 * S + S8 + s); };
-  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 2 * S8 + 7 * g + k); };
+  auto gbar = [&](int g, int k) { return bars + 8u * (1 + 2 * S + 2 * S8 + 8 * g + k); };
   auto s_full = [&](int g) { return gbar(g, 0); };
   auto s_free = [&](int g) { return gbar(g, 1); };
   auto p_full = [&](int g, int i) { return gbar(g, 2 + i); };
   auto pv_done = [&](int g, int i) { return gbar(g, 4 + i); };
   auto drain = [&](int g) { return gbar(g, 6); };
+  auto q_ready = [&](int g) { return gbar(g, 7); };  // FP8: Q tile g converted to f16
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lt::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Lt::kOffMisc + 4);
   int* s_info = reinterpret_cast<int*>(smem + Lt::kOffMisc + 8);
@@ -313,6 +323,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
           mbar_init(pv_done(g, i), 1);
         }
         mbar_init(drain(g), 1);
+        mbar_init(q_ready(g), kRows);
       }
       *s_abort = 0;
       fence_barrier_init();
@@ -455,8 +466,8 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
         const uint32_t xs[4] = {x0, x1, x2, x3};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          w[2 * q] = e4m3x2_to_bf16x2((uint16_t)(xs[q] & 0xFFFFu));
-          w[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(xs[q] >> 16));
+          w[2 * q] = e4m3x2_to_f16x2((uint16_t)(xs[q] & 0xFFFFu));
+          w[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(xs[q] >> 16));
         }
         // elements 16c .. 16c+15 -> half c / 4, 8-element chunks 2(c % 4) and 2(c % 4) + 1
         const int cc = (c & 3) * 2;
@@ -486,8 +497,10 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     const bool leader = elect_one() != 0;
     bool issued_any = false;
     if (n_kv > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kRows, 64, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16_f32(kRows, 128, false, true);
+      constexpr uint32_t kIdS =
+          FP8 ? idesc_f16_f32(kRows, 64, false, false) : idesc_bf16_f32(kRows, 64, false, false);
+      constexpr uint32_t kIdPV =
+          FP8 ? idesc_f16_f32(kRows, 128, false, true) : idesc_bf16_f32(kRows, 128, false, true);
       const uint64_t qd = smem_desc_sw128(sQ + g * kQBytes, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sKV, 16, 1024);
       // V: MN-major; 64-column halves 8 KB apart, 8-token row groups 1 KB apart
@@ -539,7 +552,9 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       };
       // software pipeline: S(j+1) runs on the tensor cores while the softmax
       // warps work on tile j; P(j) V_j follows once P(j) is written
-      bool ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
+      // Q in shared memory: as landed (BF16), or once the softmax warps have
+      // converted it to f16 (FP8)
+      bool ok = __all_sync(0xffffffffu, wait_bar(FP8 ? q_ready(g) : bar_q, 0, s_abort, err, lim_ns));
       if (ok && nkg > 0) {
         ok = issue_s(0);
         issued_any = true;
@@ -578,9 +593,63 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
     // sequence (see the epilogue); uniform over the warpgroup
     const bool full = valid && nk > 0 && t0 + kExtendTileTokens * (g + 1) <= n;
     const uint32_t trow = tmem + 256u * g + ((uint32_t)((warp & 3) * 32) << 16);
-    const float sc = p.score_scale_log2;
-    float m = -INFINITY, l = 0.f;
     bool ok = nk > 0;
+    float qinv = 1.f;  // FP8: 2^-e, the scale this row's Q was converted with
+    if constexpr (FP8) {
+      // Q row r of this tile, both 64-column halves, converted in place from
+      // bf16 to f16 with 2^e putting the row's max |q| in [2^14, 2^15): f16
+      // holds every bf16 value of that range exactly. Elementwise in place,
+      // so the swizzled chunk order of the row does not matter. Every thread
+      // arrives on q_ready, with or without work, so the MMA warp's wait ends.
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bar_q, 0, s_abort, err, lim_ns));
+      if (ok) {
+        const uint32_t qrow = sQ + g * kQBytes + r * 128;
+        // the 16 chunks of the row (2 halves x 8): read for the max, then
+        // read again, converted and written back (registers stay free). Row r
+        // takes its chunks in the order i ^ (r % 8), so the 8 rows served by
+        // one shared-memory wavefront hit 8 different bank groups.
+        auto chunk = [&](int i) {
+          return qrow + (i >> 3) * (kQBytes / 2) + ((uint32_t)((i & 7) ^ (r & 7)) << 4);
+        };
+        float mx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          uint32_t x[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                       : "r"(chunk(i)));
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            mx = fmax3(mx, fabsf(__uint_as_float(x[e] << 16)),
+                       fabsf(__uint_as_float(x[e] & 0xFFFF0000u)));
+        }
+        int e2 = 0;
+        if (mx > 0.f) {
+          e2 = 14 - ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127);
+          e2 = e2 < -100 ? -100 : (e2 > 100 ? 100 : e2);
+        }
+        const float qs = __uint_as_float((uint32_t)(127 + e2) << 23);
+        qinv = __uint_as_float((uint32_t)(127 - e2) << 23);
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          uint32_t x[4], y[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                       : "r"(chunk(i)));
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            y[e] = pack_f16(__uint_as_float(x[e] << 16) * qs,
+                            __uint_as_float(x[e] & 0xFFFF0000u) * qs);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(chunk(i)), "r"(y[0]),
+                       "r"(y[1]), "r"(y[2]), "r"(y[3])
+                       : "memory");
+        }
+        fence_async_shared();  // the S MMAs read Q through the async proxy
+      }
+      mbar_arrive(q_ready(g));
+    }
+    const float sc = p.score_scale_log2 * qinv;
+    float m = -INFINITY, l = 0.f;
     for (int j = 0; ok && j < nk; ++j) {
       ok = __all_sync(0xffffffffu, wait_bar(s_full(g), j & 1, s_abort, err, lim_ns));
       if (!ok) break;
@@ -624,7 +693,7 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
         unpack2(ffma2(pack2(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
         acc2[c & 3] = fadd2(acc2[c & 3], pack2(p0, p1));
-        pk[c] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c + 1
+        pk[c] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);  // keys 2c (low half) and 2c + 1
       }
       float r0, r1;
       unpack2(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);

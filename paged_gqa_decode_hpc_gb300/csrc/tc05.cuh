@@ -217,6 +217,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool a_mn_ma
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
          ((uint32_t)(m >> 4) << 24);
 }
+// The same with both A and B in fp16 (A / B format fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 
 }  // namespace tc05
 }  // namespace hpc

@@ -10,7 +10,9 @@ earlier operation of the same issuing warp has completed.
 Checked: no wait ever passes on a stale phase (the parity matches but the
 phase waited for has not completed), no buffer is overwritten before its
 reader is done (K/V and e4m3 ring slots, the single S buffer, the two P
-buffers, O during a rescale), every role finishes (no deadlock). The model
+buffers, O during a rescale), with an FP8 cache no S MMA reads a Q tile
+before its softmax warps have converted it to f16, every role finishes (no
+deadlock). The model
 mirrors the kernel's waits one for one; a change to either must keep them in
 step."""
 import random
@@ -48,6 +50,9 @@ class Model:
         self.S, self.S8 = stages, stages8
         B = Barrier
         self.q_full = B("q_full", 1)
+        # FP8: the softmax warps of tile g convert its Q rows to f16 in place
+        self.q_ready = [B(f"q_ready{g}", 1) for g in range(qt)]
+        self.q_f16 = [False] * qt
         self.kv_full = [B(f"kv_full{s}", 1) for s in range(stages)]
         self.kv_empty = [B(f"kv_empty{s}", qt) for s in range(stages)]
         self.kv8_full = [B(f"kv8_full{s}", 1) for s in range(stages8)]
@@ -131,11 +136,16 @@ class Model:
             m.kv_full[sb].arrive()
             yield
 
+    def q_wait(self, g):
+        # the MMA warp's wait for Q: as landed (BF16), or converted (FP8)
+        bar = self.q_ready[g] if self.fp8 else self.q_full
+        while not bar.ready(0):
+            yield WAIT
+
     def mma(self, g):
         m = self
         nkg = m.nkv[g]
-        while not m.q_full.ready(0):
-            yield WAIT
+        yield from m.q_wait(g)
 
         def issue_s(j):
             while not m.kv_full[j % m.S].ready(j // m.S):
@@ -170,6 +180,15 @@ class Model:
     def softmax(self, g):
         m = self
         nk = m.nkv[g]
+        if m.fp8:  # convert this tile's Q rows once they landed; arrive either way
+            if nk > 0:
+                while not m.q_full.ready(0):
+                    yield WAIT
+                for _ in range(m.rng.randint(1, 6)):
+                    yield
+                m.q_f16[g] = True
+            m.q_ready[g].arrive()
+            yield
         for j in range(nk):
             while not m.s_full[g].ready(j):
                 yield WAIT
@@ -210,6 +229,7 @@ class Model:
             m.__dict__.setdefault("_running", {})[g] = [m.rng.randint(1, 4)]
             if kind == "S":
                 assert m.slot[j % m.S] == j, "S MMA read a K slot holding another tile"
+                assert m.q_f16[g] or not m.fp8, "S MMA read a Q tile not yet converted"
                 assert m.S_read[g], "S buffer overwritten before the softmax copied it"
             else:
                 assert m.P_buf[g][j & 1] == j, "P*V read a P buffer holding another tile"
@@ -316,8 +336,7 @@ def _mma_with(skip_waits_for_tile=True, wait_s_free=True):
     def mma(self, g):
         m = self
         nkg = m.nkv[g]
-        while not m.q_full.ready(0):
-            yield WAIT
+        yield from m.q_wait(g)
 
         def issue_s(j):
             while not m.kv_full[j % m.S].ready(j // m.S):
@@ -387,3 +406,22 @@ def test_model_reports_a_deadlock():
                 yield WAIT
     with pytest.raises(AssertionError, match="deadlock"):
         Model.run(Stuck(random.Random(5), 1, False, [3], 6, 0))
+
+
+def test_model_catches_an_unconverted_q_read():
+    # with an FP8 cache the MMA warp waiting for the Q copy instead of the
+    # softmax warps' conversion lets an S MMA read bf16 Q as f16
+    class EarlyQ(Model):
+        def q_wait(self, g):
+            while not self.q_full.ready(0):
+                yield WAIT
+    rng = random.Random(13)
+    caught = False
+    for trial in range(300):
+        qt = rng.choice([1, 2])
+        try:
+            EarlyQ(random.Random(rng.random()), qt, True, tile_counts(rng, qt), 3, 4).run()
+        except AssertionError:
+            caught = True
+            break
+    assert caught

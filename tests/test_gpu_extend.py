@@ -92,6 +92,28 @@ def test_sharp_softmax_and_explicit_scale():
                       label=f"sharp scale={scale} tiles/CTA {tpc}")
 
 
+def test_fp8_cache_query_rows_of_any_scale():
+    # with an e4m3 cache each query row is converted to f16 with its own power
+    # of two; rows scaled by 2^-40 .. 2^3 (a flat to a sharp softmax; larger
+    # logits would put the lse beyond fp32's absolute 1e-3) must still match
+    # the oracle, and a whole q scaled by a power of two gives the same bits as
+    # the same scale in the softmax scale argument
+    w = W.make_workload(_cfg(64, 8, True), lengths=[700, 129], seed=48)
+    q, cu = W.make_extend_query(w, [300, 129], seed=49, q_scale=4.0)
+    gen = torch.Generator().manual_seed(50)
+    pw = torch.randint(-40, 4, q.shape[:2], generator=gen).to(torch.float32)
+    qs = (q.float() * torch.exp2(pw)[..., None]).to(torch.bfloat16)
+    for tpc in (1, 2):
+        out, lse = run_extend(w, qs, cu, tpc=tpc)
+        ref_out, ref_lse = _oracle(w, qs, cu)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      label=f"fp8 cache, rows scaled 2^-40..2^3, tiles/CTA {tpc}")
+    q3 = (q.float() * 8.0).to(torch.bfloat16)  # exact: a power of two
+    out1, _ = run_extend(w, q, cu, softmax_scale=w.softmax_scale * 8.0)
+    out2, _ = run_extend(w, q3, cu)
+    assert torch.equal(out1, out2)
+
+
 def test_block_permutation_and_layout_invariance():
     w = W.make_workload(_cfg(64, 8), lengths=[300, 77], seed=44, slack_blocks=5)
     q, cu = W.make_extend_query(w, [120, 40], seed=45)
