@@ -30,9 +30,12 @@
 //    in shared memory), and CTAs with no static part start on the pool.
 //
 // Roles: 1 producer warp (pieces, block-table reads, TMA copies of each
-// (tile, KV head) K and V tile into a STAGES-deep ring) and 8 consumer warps
+// (tile, KV head) K and V tile into a STAGES-deep ring), 8 consumer warps
 // (the unit math of decode_common.cuh: S^T = K Q^T and O^T += V^T P^T on
-// mma.sync with the online softmax in registers). Every wait is bounded; on a
+// mma.sync with the online softmax in registers) and 2 epilogue warps taking
+// alternate pieces (combine, final or partial writes, arrival counts and
+// merges, whose global round trips would otherwise queue behind each other
+// at the end of the step). Every wait is bounded; on a
 // timeout the CTA keeps walking and publishing its pieces without copies, so
 // the arrival counters and the pool still return to zero.
 #include <cuda_bf16.h>
@@ -46,7 +49,7 @@ namespace hpc {
 namespace {
 
 constexpr int kSNC = 8;                           // consumer warps
-constexpr int kEpilogueWarps = 1;                 // epilogue warps, taking pieces in turn
+constexpr int kEpilogueWarps = 2;                 // epilogue warps, taking pieces in turn
 constexpr int kProducerWarp = kSNC, kEpilogueWarp0 = kSNC + 1;
 constexpr int kSThreads = (kSNC + 1 + kEpilogueWarps) * 32;
 constexpr int kPieceQ = 4;                        // piece descriptors in flight
