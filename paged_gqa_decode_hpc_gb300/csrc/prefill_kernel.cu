@@ -80,8 +80,8 @@ struct Layout {
   static constexpr int kConvWarp0 = 4 * QT;
   static constexpr int kProducerWarp = 4 * QT + kConvWarps, kMmaWarp0 = kProducerWarp + 1;
   static constexpr int kThreads = 32 * (kMmaWarp0 + QT);
-  static constexpr int kStages = FP8 ? 3 : (QT == 1 ? 6 : 5);            // bf16 K+V ring
-  static constexpr int kStages8 = FP8 ? (QT == 1 ? 6 : 4) : 0;           // e4m3 K+V ring
+  static constexpr int kStages = FP8 ? 4 : (QT == 1 ? 6 : 5);            // 16-bit K+V ring
+  static constexpr int kStages8 = FP8 ? (QT == 1 ? 4 : 2) : 0;           // e4m3 K+V ring
   static constexpr uint32_t kOffQ = 0;                                   // QT x 32 KB
   static constexpr uint32_t kOffKV = QT * kQBytes;                       // stages x 32 KB
   static constexpr uint32_t kOffKV8 = kOffKV + kStages * kStageBytes;    // stages8 x 16 KB

@@ -90,10 +90,15 @@ struct StepCfg {
   static constexpr int kSmemBytesMax = kSmemBytes + 4 * (kStepMaxSeqs + 1);
 };
 
-// Orders this thread's earlier writes before its later ones at device scope
-// (release / acquire), lighter than a sequentially consistent fence.
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+// atomicAdd with acquire-release semantics at device scope: the writes that
+// happen before it (this thread's, and the warp's through a warp barrier)
+// are visible before the addition, and reads after it see what the earlier
+// releasers wrote.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int prev;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(prev) : "l"(p), "r"(v)
+               : "memory");
+  return prev;
 }
 
 template <bool FP8>
@@ -164,7 +169,7 @@ constexpr int kPartFloat4 = kDepSlices * 32;
 // The warp that counts the last piece of a split pair merges the pair's k
 // partial states in owner order (M = max m_i, l = sum l_i 2^(m_i - M),
 // out = sum o_i 2^(m_i - M) / l). They were written by other CTAs, which
-// fenced before counting themselves, and are read from L2 (.cg), never L1.
+// released them with their count, and are read from L2 (.cg), never L1.
 template <bool FP8>
 __device__ __forceinline__ void merge_pair(const StepParams& p, const StepMath& M,
                                            const int32_t* cu, int b, int h, int lane) {
@@ -581,19 +586,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
         pd[dm * 32] = make_float4(acc[dm][0] * p.v_scale, acc[dm][1] * p.v_scale,
                                   acc[dm][2] * p.v_scale, acc[dm][3] * p.v_scale);
       pd[8 * 32] = make_float4(M0, M1, L0, L1);
-      fence_acq_rel_gpu();  // this partial is visible device-wide before the pair is counted
+      // One acquire-release atomic by lane 0 counts the piece: its release
+      // covers the whole warp's partial writes (ordered before it by the
+      // warp barrier), its acquire the other pieces' partials, which the
+      // warp's merge reads after the second warp barrier.
       __syncwarp();
       int last = 0;
       if (lane == 0) {
         int32_t* cnt = p.pair_cnt + (int64_t)b * H + h;
-        last = atomicAdd(cnt, 1) == (fl >> 8) - 1;
+        last = atom_add_acq_rel_gpu(cnt, 1) == (fl >> 8) - 1;
         if (last) *cnt = 0;  // every piece of the pair has arrived: ready for the next step
       }
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        fence_acq_rel_gpu();  // acquire: every other piece's partial is visible
-        merge_pair<FP8>(p, M, cu, b, h, lane);
-      }
+      __syncwarp();
+      if (last) merge_pair<FP8>(p, M, cu, b, h, lane);
     }
     named_bar_sync(3, kSThreads);
     return;

@@ -299,8 +299,8 @@ def tile_counts(rng, qt):
 @pytest.mark.parametrize("qt,fp8", [(1, False), (2, False), (1, True), (2, True)])
 def test_protocol_random_interleavings(qt, fp8):
     rng = random.Random(1234 + 10 * qt + fp8)
-    stages = (3 if fp8 else (6 if qt == 1 else 5))
-    stages8 = (6 if qt == 1 else 4) if fp8 else 0
+    stages = (4 if fp8 else (6 if qt == 1 else 5))
+    stages8 = (4 if qt == 1 else 2) if fp8 else 0
     for trial in range(300):
         nkv = tile_counts(rng, qt)
         Model(random.Random(rng.random()), qt, fp8, nkv, stages, stages8).run()
