@@ -611,7 +611,9 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
         auto chunk = [&](int i) {
           return qrow + (i >> 3) * (kQBytes / 2) + ((uint32_t)((i & 7) ^ (r & 7)) << 4);
         };
-        float mx = 0.f;
+        // max |q| of the row on packed pairs: max.xorsign.abs gives the larger
+        // magnitude of each half (its sign is dropped below)
+        uint32_t m2[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           uint32_t x[4];
@@ -620,9 +622,13 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
                        : "r"(chunk(i)));
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            mx = fmax3(mx, fabsf(__uint_as_float(x[e] << 16)),
-                       fabsf(__uint_as_float(x[e] & 0xFFFF0000u)));
+            asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2[e]) : "r"(m2[e]), "r"(x[e]));
         }
+        float mx = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          mx = fmax3(mx, fabsf(__uint_as_float(m2[e] << 16)),
+                     fabsf(__uint_as_float(m2[e] & 0xFFFF0000u)));
         int e2 = 0;
         if (mx > 0.f) {
           e2 = 14 - ((int)((__float_as_uint(mx) >> 23) & 0xFF) - 127);
