@@ -15,10 +15,15 @@
 // Design (the extend kernel's pipeline, made persistent over segments):
 //  * CTA = (KV head h, plan part y); it walks the part's segments (sequence
 //    b, tiles [tb, te)) in order. Warps: 4 softmax warps (thread = query row
-//    = TMEM lane; row 8t + g is token t, query head g), 8 e4m3 -> bf16
-//    converter warps (FP8 caches only: widening, not HBM, sets the FP8 tile
-//    rate, and 8 warps widen a tile in half the time of 4), 1 TMA producer
-//    warp, 1 MMA warp.
+//    = TMEM lane; row 8t + g is token t, query head g), 8 e4m3 -> f16
+//    converter warps (FP8 caches only: 8 warps widen a tile in half the time
+//    of 4), 1 TMA producer warp, 1 MMA warp.
+//  * FP8 caches run the MMAs in fp16: every e4m3 value is an f16 value (one
+//    conversion per pair); at the start of each segment every softmax thread
+//    converts its own Q row in place to f16 with a power-of-two scale putting
+//    the row's max |q| in [2^14, 2^15) and keeps the inverse for its logit
+//    scale; P is packed as f16. The MMA warp starts a segment's S MMAs once
+//    every softmax thread has arrived on q_ready.
 //  * Q of a segment: one TMA per 64-column half (box 64 x 8 heads x q_len
 //    tokens, 128-byte swizzle) into one of two 16 KB Q slots, so the next
 //    segment's Q loads while this one finishes. Rows past 8 q_len are never
@@ -28,7 +33,7 @@
 //    barrier phases count tiles over the whole CTA, across segments.
 //  * S_j = Q K_j^T (M 128, N 64, K 128) into tensor memory; online softmax in
 //    the log2 domain with the running maximum moved only when it grows by
-//    more than 8 (P = 2^(s - m) < 256); P (bf16) back to tensor memory;
+//    more than 8 (P = 2^(s - m) < 256); P (16-bit) back to tensor memory;
 //    O += P V_j (M 128, N 128, K 64) with A = P from tensor memory and V as
 //    the MN-major operand. The first P V of a segment (accumulate off)
 //    overwrites O: it waits for P of the segment's first tile, which the
@@ -82,8 +87,8 @@ struct TcLayout {
   static constexpr uint32_t kOffKV8 = kOffKV + kStages * kStageBytes;
   static constexpr uint32_t kOffBar = kOffKV8 + kStages8 * kStageBytes8;
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], kv8_full[S8], kv8_empty[S8],
-  // s_full, s_free, p_full[2], pv_done[2], drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 2 * kStages8 + 7;
+  // s_full, s_free, p_full[2], pv_done[2], drain, q_ready[2]
+  static constexpr int kNumBars = 4 + 2 * kStages + 2 * kStages8 + 9;
   static constexpr uint32_t kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align to 1024
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -123,12 +128,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 // Two e4m3 bytes (low byte -> low half) to bf16x2, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t x) {
+// Two e4m3 bytes (low byte -> low half) to f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
   uint32_t h;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(x));
-  const float lo = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
-  const float hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
-  return pack_bf16(lo, hi);
+  return h;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -195,6 +204,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
   auto p_full = [&](int i) { return bar1 + 16u + 8u * i; };
   auto pv_done = [&](int i) { return bar1 + 32u + 8u * i; };
   const uint32_t drain = bar1 + 48;
+  auto q_ready = [&](int i) { return bar1 + 56u + 8u * i; };  // FP8: Q slot i converted
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Lt::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Lt::kOffMisc + 4);
 
@@ -225,6 +235,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         mbar_init(pv_done(i), 1);
       }
       mbar_init(drain, 1);
+      for (int i = 0; i < 2; ++i) mbar_init(q_ready(i), kRows);
       *s_abort = 0;
       fence_barrier_init();
       prefetch_map(&tmq);
@@ -384,8 +395,8 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
           const uint32_t xs[4] = {x0, x1, x2, x3};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            w[2 * q] = e4m3x2_to_bf16x2((uint16_t)(xs[q] & 0xFFFFu));
-            w[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(xs[q] >> 16));
+            w[2 * q] = e4m3x2_to_f16x2((uint16_t)(xs[q] & 0xFFFFu));
+            w[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(xs[q] >> 16));
           }
           const int cc = (c & 3) * 2;
           const uint32_t row = kb + mat * kKVTileBytes + (c >> 2) * (kKVTileBytes / 2) + t * 128;
@@ -411,8 +422,10 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
     // elected lane issues the MMAs and commits.
     const bool leader = elect_one() != 0;
     bool issued_any = false;
-    constexpr uint32_t kIdS = idesc_bf16_f32(kRows, 64, false, false);
-    constexpr uint32_t kIdPV = idesc_bf16_f32(kRows, 128, false, true);
+    constexpr uint32_t kIdS =
+        FP8 ? idesc_f16_f32(kRows, 64, false, false) : idesc_bf16_f32(kRows, 64, false, false);
+    constexpr uint32_t kIdPV =
+        FP8 ? idesc_f16_f32(kRows, 128, false, true) : idesc_bf16_f32(kRows, 128, false, true);
     const uint64_t kd0 = smem_desc_sw128(sKV, 16, 1024);
     // V: MN-major; 64-column halves 8 KB apart, 8-token row groups 1 KB apart
     const uint64_t vd0 = smem_desc_sw128(sKV + kKVTileBytes, kKVTileBytes / 2, 1024);
@@ -465,8 +478,9 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
       const Seg sgm = read_seg(p, sg);
       const int n = sgm.te - sgm.tb;
       if (n <= 0) continue;
-      ok = __all_sync(0xffffffffu,
-                      wait_bar(q_full(k & 1), (k >> 1) & 1, s_abort, err, lim_ns));
+      // Q of the segment: as landed (BF16), or converted to f16 (FP8)
+      ok = __all_sync(0xffffffffu, wait_bar(FP8 ? q_ready(k & 1) : q_full(k & 1), (k >> 1) & 1,
+                                            s_abort, err, lim_ns));
       if (!ok) break;
       const uint64_t qd = smem_desc_sw128(sQ + (uint32_t)(k & 1) * kQSlotBytes, 16, 1024);
       // software pipeline: S(g+1) runs while the softmax warps work on tile g;
@@ -498,7 +512,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
     // barrier counts (their S, P and O rows are never read)
     const bool live = 32 * warp < kGroupRows * T;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const float sc = p.score_scale_log2;
+    const float sc0 = p.score_scale_log2;
     bool ok = true;
     int G = 0, k = 0;
     for (int sg = sg0; sg < sg1 && ok; ++sg) {
@@ -511,6 +525,61 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
       // are not masked (their values are never read) so that a warp holding
       // some of them does not run the masking loop on every tile.
       const int lim = row_ok ? L - (T - 1 - t) : 0x7FFFFFFF;
+      float sc = sc0;
+      if constexpr (FP8) {
+        // this segment's Q row, both 64-column halves, converted in place from
+        // bf16 to f16 with 2^e putting the row's max |q| in [2^14, 2^15) (f16
+        // holds every bf16 value of that range exactly); chunk i of row r in
+        // the order i ^ (r % 8), so one shared-memory wavefront's 8 rows hit 8
+        // bank groups. Every thread arrives on q_ready, with a row or not.
+        ok = __all_sync(0xffffffffu, wait_bar(q_full(k & 1), (k >> 1) & 1, s_abort, err, lim_ns));
+        if (ok && row_ok) {
+          const uint32_t qrow = sQ + (uint32_t)(k & 1) * kQSlotBytes + (uint32_t)r * 128;
+          auto chunk = [&](int i) {
+            return qrow + (i >> 3) * kQHalfBytes + ((uint32_t)((i & 7) ^ (r & 7)) << 4);
+          };
+          uint32_t m2[4] = {0u, 0u, 0u, 0u};  // larger magnitude per half (sign dropped below)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            uint32_t x[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                         : "r"(chunk(i)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2[e]) : "r"(m2[e]), "r"(x[e]));
+          }
+          float mq = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            mq = fmax3(mq, fabsf(__uint_as_float(m2[e] << 16)),
+                       fabsf(__uint_as_float(m2[e] & 0xFFFF0000u)));
+          int e2 = 0;
+          if (mq > 0.f) {
+            e2 = 14 - ((int)((__float_as_uint(mq) >> 23) & 0xFF) - 127);
+            e2 = e2 < -100 ? -100 : (e2 > 100 ? 100 : e2);
+          }
+          const float qs = __uint_as_float((uint32_t)(127 + e2) << 23);
+          sc = sc0 * __uint_as_float((uint32_t)(127 - e2) << 23);
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {
+            uint32_t x[4], y[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                         : "r"(chunk(i)));
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              y[e] = pack_f16(__uint_as_float(x[e] << 16) * qs,
+                              __uint_as_float(x[e] & 0xFFFF0000u) * qs);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(chunk(i)), "r"(y[0]),
+                         "r"(y[1]), "r"(y[2]), "r"(y[3])
+                         : "memory");
+          }
+          fence_async_shared();  // the S MMAs read Q through the async proxy
+        }
+        mbar_arrive(q_ready(k & 1));
+        if (!ok) break;
+      }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; ok && j < n; ++j) {
         const int g = G + j;
@@ -560,7 +629,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
             unpack2(ffma2(pack2(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
             acc2[c & 3] = fadd2(acc2[c & 3], pack2(p0, p1));
-            pk[c] = pack_bf16(p0, p1);  // keys 2c (low half) and 2c + 1
+            pk[c] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);  // keys 2c (low) and 2c + 1
           }
           float r0, r1;
           unpack2(fadd2(fadd2(acc2[0], acc2[1]), fadd2(acc2[2], acc2[3])), r0, r1);

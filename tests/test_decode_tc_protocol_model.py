@@ -9,7 +9,10 @@ of the issuing warp has completed.
 
 Checked, across segment boundaries: no wait passes on a stale phase, no
 buffer is overwritten before its reader is done (the two Q slots, K/V and
-e4m3 ring slots, the single S buffer, the two P buffers), the first P V of a
+e4m3 ring slots, the single S buffer, the two P buffers), with an FP8
+cache no S MMA reads a Q slot before the softmax warps converted it to f16
+for its segment and no Q slot is reloaded while it is being converted, the
+first P V of a
 segment does not overwrite O before the previous segment's epilogue read it
 (the kernel has no barrier for this: that P V waits for P of the segment's
 first tile, which the softmax warps write after their epilogue), each
@@ -51,6 +54,10 @@ class Model:
         B = Barrier
         self.q_full = [B(f"q_full{i}", 1) for i in range(2)]
         self.q_empty = [B(f"q_empty{i}", 1) for i in range(2)]
+        # FP8: the softmax warps convert a segment's Q slot to f16 in place
+        self.q_ready = [B(f"q_ready{i}", 1) for i in range(2)]
+        self.q_conv = [None, None]          # segment whose Q a slot holds as f16
+        self.q_converting = [False, False]
         self.kv_full = [B(f"kv_full{s}", 1) for s in range(stages)]
         self.kv_empty = [B(f"kv_empty{s}", 1) for s in range(stages)]
         self.kv8_full = [B(f"kv8_full{s}", 1) for s in range(stages8)]
@@ -90,9 +97,11 @@ class Model:
                 while not m.q_empty[k & 1].ready((k >> 1) - 1):
                     yield WAIT
             assert m.q_reads[k & 1] == 0, "Q slot overwritten while an S MMA reads it"
+            assert not m.q_converting[k & 1], "Q slot overwritten while being converted"
 
             def land_q(k=k):
                 m.q_slot[k & 1] = k
+                m.q_conv[k & 1] = None
                 m.q_full[k & 1].arrive()
             m.tma.append((m.tick + m.rng.randint(1, 20), land_q))
             yield
@@ -171,12 +180,17 @@ class Model:
         m.pipe.append(("commit", m.kv_empty[g % m.S]))
         yield
 
+    def q_wait(self, k):
+        # the MMA warp's wait for a segment's Q: as landed (BF16) or converted (FP8)
+        bar = (self.q_ready if self.fp8 else self.q_full)[k & 1]
+        while not bar.ready(k >> 1):
+            yield WAIT
+
     def mma(self):
         m = self
         G = 0
         for k, n in enumerate(m.segs):
-            while not m.q_full[k & 1].ready(k >> 1):
-                yield WAIT
+            yield from m.q_wait(k)
             yield from m.issue_s(G, k, (k & 1) if n == 1 else None)
             for j in range(n):
                 if j + 1 < n:
@@ -188,6 +202,17 @@ class Model:
         m = self
         G = 0
         for k, n in enumerate(m.segs):
+            if m.fp8:  # convert this segment's Q rows once they landed
+                while not m.q_full[k & 1].ready(k >> 1):
+                    yield WAIT
+                assert m.q_slot[k & 1] == k, "converted a Q slot holding another segment"
+                m.q_converting[k & 1] = True
+                for _ in range(m.rng.randint(1, 5)):
+                    yield
+                m.q_converting[k & 1] = False
+                m.q_conv[k & 1] = k
+                m.q_ready[k & 1].arrive()
+                yield
             for j in range(n):
                 g = G + j
                 while not m.s_full.ready(g):
@@ -239,6 +264,7 @@ class Model:
                 _, g, k = op
                 assert m.slot[g % m.S] == g, "S MMA read a K slot holding another tile"
                 assert m.q_slot[k & 1] == k, "S MMA read a Q slot holding another segment"
+                assert not m.fp8 or m.q_conv[k & 1] == k, "S MMA read a Q slot not yet converted"
                 assert m.S_read, "S buffer overwritten before the softmax copied it"
                 m.q_reads[k & 1] += 1
             else:
@@ -317,7 +343,7 @@ def random_segments(rng):
 @pytest.mark.parametrize("fp8", [False, True])
 def test_protocol_random_interleavings(fp8):
     rng = random.Random(4321 + fp8)
-    stages, stages8 = (3, 6) if fp8 else (6, 0)
+    stages, stages8 = (4, 4) if fp8 else (6, 0)
     for trial in range(400):
         Model(random.Random(rng.random()), fp8, random_segments(rng), stages, stages8).run()
 
@@ -326,7 +352,7 @@ def test_protocol_random_interleavings(fp8):
 def test_protocol_single_tile_segments(fp8):
     # every segment one tile: Q slots and O turn over on every tile
     rng = random.Random(99 + fp8)
-    stages, stages8 = (3, 6) if fp8 else (6, 0)
+    stages, stages8 = (4, 4) if fp8 else (6, 0)
     for trial in range(200):
         Model(random.Random(rng.random()), fp8, [1] * rng.randint(2, 9), stages, stages8).run()
 
@@ -417,3 +443,21 @@ def test_model_reports_a_deadlock():
                 yield WAIT
     with pytest.raises(AssertionError, match="deadlock"):
         Stuck(random.Random(5), False, [3, 2], 6, 0).run()
+
+
+def test_model_catches_an_unconverted_q_read():
+    # with an FP8 cache, an MMA warp that starts a segment on the Q copy
+    # instead of the softmax warps' conversion reads bf16 Q as f16
+    class EarlyQ(Model):
+        def q_wait(self, k):
+            while not self.q_full[k & 1].ready(k >> 1):
+                yield WAIT
+    rng = random.Random(29)
+    caught = False
+    for trial in range(400):
+        try:
+            EarlyQ(random.Random(rng.random()), True, random_segments(rng), 4, 4).run()
+        except AssertionError:
+            caught = True
+            break
+    assert caught

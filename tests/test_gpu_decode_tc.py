@@ -94,6 +94,22 @@ def test_tc_parity(T, hq, hkv, fp8, plan, sms):
     assert_parity(out, lse, ref_out, ref_lse, label=f"tc T={T} hkv={hkv} fp8={fp8} {plan}")
 
 
+@pytest.mark.parametrize("T", [4, 8])
+def test_tc_fp8_query_rows_of_any_scale(T):
+    # with an e4m3 cache each query row is converted to f16 with its own power
+    # of two at the start of each segment; rows scaled by 2^-40 .. 2^3 (a flat
+    # to a sharp softmax) must match the oracle under both plans
+    w = W.make_workload(_cfg(64, 8, True), lengths=LENS, seed=73, slack_blocks=2)
+    q = W.make_multi_query(w, T, seed=74)
+    gen = torch.Generator().manual_seed(75)
+    pw = torch.randint(-40, 4, q.shape[:3], generator=gen).to(torch.float32)
+    q = (q.float() * 4.0 * torch.exp2(pw)[..., None]).to(torch.bfloat16)
+    ref_out, ref_lse = _oracle(w, q)
+    for plan, sms in (("step", None), ("host", 7)):
+        out, lse = run(w, q, plan=plan, num_sms=sms)
+        assert_parity(out, lse, ref_out, ref_lse, label=f"tc fp8 T={T} rows 2^-40..2^3 {plan}")
+
+
 @pytest.mark.parametrize("fp8", [False, True])
 def test_tc_one_tile_per_part(fp8):
     # every part one tile: each CTA walks one-tile segments, so Q slots turn
