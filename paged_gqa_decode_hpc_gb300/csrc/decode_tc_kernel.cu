@@ -359,15 +359,18 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
       }
     }
   } else if (FP8 && warp >= Lt::kConvWarp0 && warp < Lt::kProducerWarp) {
-    // ------------------------------------------- e4m3 -> bf16 converters
+    // -------------------------------------------- e4m3 -> f16 converters
     // Each e4m3 tile (64 token rows x 128 bytes, 128-byte swizzle: 16-byte
-    // chunk c of row t at c ^ (t % 8)) is widened exactly into the bf16 tile
+    // chunk c of row t at c ^ (t % 8)) is widened exactly into the f16 tile
     // the MMAs read (two 64-column halves, 8-element chunk c' of row t at
-    // c' ^ (t % 8)). Threads 0..127 widen K, 128..255 V. Thread-to-chunk
-    // map: each group of 8 threads serving one 16-byte access covers all 8
-    // bank groups on the load and both stores.
-    const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. 255
-    const int mat = ct >> 7, ctl = ct & 127;
+    // c' ^ (t % 8)). With 8 warps threads 0..127 widen K and 128..255 V; with
+    // 4 warps each thread takes a K item, then a V item. Thread-to-chunk map:
+    // each group of 8 threads serving one 16-byte access covers all 8 bank
+    // groups on the load and both stores.
+    constexpr int kNT = FP8 ? 32 * Lt::kConvWarps : 256;  // (no converters with a bf16 cache)
+    static_assert(kNT == 128 || kNT == 256, "4 or 8 converter warps");
+    const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. kNT - 1
+    const int ctl = ct & 127;
     const int cq = ctl & 15, c = cq & 7, cr = ((cq >> 2) & 1) ^ (cq >> 3);
     bool ok = true;
     int G = 0;
@@ -385,8 +388,9 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
         if (!ok) break;
         const uint32_t e8 = sKV8 + s8 * kStageBytes8, kb = sKV + sb * kStageBytes;
 #pragma unroll 2
-        for (int it = 0; it < 4; ++it) {
-          const int t = it * 16 + (ctl >> 4) * 2 + cr;
+        for (int it = 0; it < 1024 / kNT; ++it) {
+          const int mat = kNT == 256 ? ct >> 7 : it >> 2;
+          const int t = (it & 3) * 16 + (ctl >> 4) * 2 + cr;
           uint32_t x0, x1, x2, x3;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                        "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                        : "memory");
         }
-        fence_async_shared();  // the MMAs read the bf16 tile through the async proxy
+        fence_async_shared();  // the MMAs read the f16 tile through the async proxy
         mbar_arrive(kv8_empty(s8));
         mbar_arrive(kv_full(sb));
       }

@@ -431,14 +431,17 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       }
     }
   } else if (FP8 && warp >= Lt::kConvWarp0 && warp < Lt::kProducerWarp) {
-    // ------------------------------------------- e4m3 -> bf16 converters
+    // -------------------------------------------- e4m3 -> f16 converters
     // Each e4m3 tile (64 token rows x 128 bytes, 128-byte swizzle: 16-byte
     // chunk c of row t at c ^ (t % 8)) is widened exactly (e4m3 values are
-    // bf16 values) into the bf16 tile the MMAs read: two 64-column halves,
+    // f16 values) into the f16 tile the MMAs read: two 64-column halves,
     // 8-element chunk c' of row t at c' ^ (t % 8). The scales stay out:
     // k_scale is in the logit scale, v_scale in the epilogue.
-    const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. 127
-    // Work item it (0 .. 7) of thread ct: matrix it / 4, row t, 16-byte chunk
+    constexpr int kNT = FP8 ? 32 * Lt::kConvWarps : 128;  // (no converters with a bf16 cache)
+    static_assert(kNT == 64 || kNT == 128, "2 or 4 converter warps");
+    constexpr int kRowSteps = 1024 / kNT / 2;  // items per matrix: rows t in kRowSteps bands
+    const int ct = threadIdx.x - 32 * Lt::kConvWarp0;  // 0 .. kNT - 1
+    // Work item it of thread ct: matrix it / kRowSteps, row t, 16-byte chunk
     // c. A 16-byte shared access is served 8 threads at a time; each such
     // group takes four chunks of one row and the other four of a row of the
     // opposite swizzle parity, so its e4m3 loads and both of its bf16 stores
@@ -456,8 +459,9 @@ __global__ void __launch_bounds__(Layout<QT, FP8>::kThreads, 1)
       if (!ok) break;
       const uint32_t e8 = sKV8 + s8 * kStageBytes8, kb = sKV + sb * kStageBytes;
 #pragma unroll 2
-      for (int it = 0; it < 8; ++it) {
-        const int mat = it >> 2, t = (it & 3) * 16 + (ct >> 4) * 2 + cr;
+      for (int it = 0; it < 2 * kRowSteps; ++it) {
+        const int mat = it / kRowSteps;
+        const int t = (it % kRowSteps) * (64 / kRowSteps) + (ct >> 4) * 2 + cr;
         uint32_t x0, x1, x2, x3;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
