@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(TcLayout<FP8>::kThreads, 1)
                           wait_bar(kv_empty(sb), ((g / S) - 1) & 1, s_abort, err, lim_ns));
         if (!ok) break;
         const uint32_t e8 = sKV8 + s8 * kStageBytes8, kb = sKV + sb * kStageBytes;
-#pragma unroll 2
+#pragma unroll 4
         for (int it = 0; it < 1024 / kNT; ++it) {
           const int mat = kNT == 256 ? ct >> 7 : it >> 2;
           const int t = (it & 3) * 16 + (ctl >> 4) * 2 + cr;
