@@ -150,6 +150,22 @@ def test_step_records_count_every_run():
     plan.destroy()
 
 
+def test_step_at_the_in_kernel_sequence_limit():
+    # 3072 sequences, the most the step kernel plans in shared memory (its
+    # prefix array fills the dynamic shared memory it is configured for),
+    # with empty sequences among them: parity, the oracle's work list, and
+    # the same bits on a second step
+    lens = [(i * 53) % 300 for i in range(3072)]
+    w = W.make_workload(_cfg(8, 1), lengths=lens, seed=44)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    out, lse, words, err = run_step(w)
+    assert err == 0
+    assert_parity(out, lse, ref_out, ref_lse, label="step 3072 seqs")
+    check_step_records(words, lens, hpc.hpc_device_sm_count(), 1)
+    out2, lse2, _, err2 = run_step(w)
+    assert err2 == 0 and np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
 def test_step_many_sequences_uses_the_planner_kernel():
     lens = [(i * 37) % 150 + 1 for i in range(3500)]  # above the in-kernel limit
     w = W.make_workload(_cfg(8, 1), lengths=lens, seed=42)
