@@ -256,20 +256,29 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
                            hpc_tensor* lse, void* stream);
 
 /*
- * hpc_decode_step -- one whole decode step on the device: the balanced plan
- * of hpc_decode_plan_device, attention and merge, with the planning folded
- * into the attention kernel's start (each CTA derives its own part from the
- * device lengths), so a step is two kernel launches (three on the
- * tensor-core multi-token path below: planner kernel, attention, merge). Afterwards `plan` holds
- * this step's work list, word for word the host planner's for the same
- * lengths (hpc_decode_plan_compute_ex, hpc_decode_plan_export): a plan of
- * one unit per (tile, KV head) (units_per_tile = num_kv_heads) when
- * num_kv_heads * q_len <= 8 and num_kv_heads > 1, else of tiles. Batches
- * above 3072 sequences run the separate planner kernel first. With q_len at
- * or above the tensor-core threshold (hpc_decode_tc_min_q_len) the planner
- * kernel builds a tile plan of max(1, num_sms / num_kv_heads) parts and the
- * tensor-core kernel runs one CTA per (KV head, part). Allocates nothing; may
- * be captured in a CUDA graph after a first call outside the capture.
+ * hpc_decode_step -- one whole decode step on the device, planned from the
+ * device lengths inside the step (section "Attention Backend: Dynamic
+ * Load-Balanced Scheduling": tiles spread over a persistent grid by actual
+ * work, partial states merged by log-sum-exp). Three routes:
+ *  - one query token per sequence (q [B][H_q][128]) and B <= 3072: one
+ *    launch of the step kernel, which plans the step (units = (tile, KV
+ *    head) pairs; balanced static parts plus a pool of chunks the CTAs take
+ *    at run time), computes it and merges every split (sequence, KV head)
+ *    pair in the kernel. Afterwards `plan` holds the step's work list as
+ *    HPC_PLAN_STEP records (hpc_decode_plan_export);
+ *  - q_len at or above the tensor-core threshold (hpc_decode_tc_min_q_len):
+ *    the planner kernel builds a tile plan of max(1, num_sms / H_kv) parts,
+ *    the tensor-core kernel runs one CTA per (KV head, part), then the merge
+ *    kernel;
+ *  - otherwise (multi-token q below the threshold, or B > 3072): the balanced
+ *    plan of hpc_decode_plan_device (folded into the attention kernel's
+ *    start up to 3072 sequences, else the planner kernel first), attention
+ *    and merge; `plan` then holds that plan's words, word for word the host
+ *    planner's for the same lengths (hpc_decode_plan_compute_ex): one unit
+ *    per (tile, KV head) when num_kv_heads * q_len <= 8 and num_kv_heads > 1,
+ *    else tiles.
+ * Allocates nothing; may be captured in a CUDA graph after a first call
+ * outside the capture.
  *   q, k_cache, v_cache, block_table, out, lse: as hpc_decode_attn
  *   seq_lens  device int32 [B], contiguous
  *   plan      from hpc_decode_plan_create with max_seqs >= B
@@ -279,6 +288,32 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
                            const hpc_tensor* v_cache, const hpc_tensor* block_table,
                            const hpc_tensor* seq_lens, hpc_plan_t plan, int32_t num_sms,
                            hpc_tensor* out, hpc_tensor* lse, void* stream);
+
+/*
+ * hpc_decode_step_host -- hpc_decode_step with the step's inputs and results
+ * in HOST memory: the copies in, the step and the copies out are enqueued on
+ * `stream` by the library (one cudaMemcpyAsync per buffer), so a caller
+ * whose batch lives on the host makes one call per step. The caches stay on
+ * the device.
+ *   q, block_table, seq_lens  host tensors, contiguous (dense, outermost
+ *                             first), same shapes and dtypes as for
+ *                             hpc_decode_step; read by the copies, which
+ *                             are asynchronous only for page-locked memory
+ *   out, lse                  host tensors, contiguous, written when the
+ *                             stream reaches the copies out (lse may be NULL)
+ *   k_cache, v_cache, plan, num_sms, stream: as hpc_decode_step
+ * The plan owns a device staging area for the five buffers; the first call
+ * (or one with a larger batch) allocates it, later calls reuse it. Host
+ * buffers must stay valid and unchanged until the stream has passed the
+ * copies; two calls on one plan must not overlap on different streams.
+ * Errors: HPC_ERR_INVALID_ARG for a null or non-contiguous host tensor (no
+ * copy enqueued), HPC_ERR_OOM if the staging area cannot be allocated,
+ * otherwise hpc_decode_step's.
+ */
+hpc_status hpc_decode_step_host(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                const hpc_tensor* seq_lens, hpc_plan_t plan, int32_t num_sms,
+                                hpc_tensor* out, hpc_tensor* lse, void* stream);
 
 /* hpc_decode_attn_ex -- hpc_decode_attn with an explicit softmax scale
  * (> 0; a value <= 0 selects 1/sqrt(head_dim)). */

@@ -25,6 +25,7 @@ __all__ = [
     "hpc_decode_plan_compute", "hpc_decode_plan_static_compute", "hpc_decode_plan_status",
     "hpc_decode_plan_destroy", "hpc_decode_attn", "hpc_device_sm_count", "hpc_last_error",
     "hpc_decode_plan_set_timing_events", "hpc_decode_attn_noalloc", "hpc_decode_step",
+    "hpc_decode_step_host",
     "hpc_rope_norm_kv_write", "hpc_extend_attn", "hpc_decode_tc_min_q_len",
     "HPC_OK", "HPC_ERR_INVALID_ARG", "HPC_ERR_UNSUPPORTED", "HPC_ERR_CUDA", "HPC_ERR_OOM",
     "HPC_ERR_DEVICE_CHECK",
@@ -103,6 +104,7 @@ def load_library():
             "hpc_decode_plan_set_timing_events": [P, P, P, P],
             "hpc_decode_attn_noalloc": [T, T, T, T, T, i32, T, T, P, P],
             "hpc_decode_step": [T, T, T, T, T, P, i32, T, T, P],
+            "hpc_decode_step_host": [T, T, T, T, T, P, i32, T, T, P],
             "hpc_decode_tc_min_q_len": [i32, pi32],
             "hpc_rope_norm_kv_write": [T, T, T, T, T, T, T, ctypes.c_float, ctypes.c_float,
                                        T, T, T, T, P, P],
@@ -369,8 +371,9 @@ def hpc_extend_attn(q, k_cache, v_cache, block_table, seq_lens, cu_q_lens, out, 
 
 def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int, out,
                     lse=None, stream=None, k_scale: float = 1.0, v_scale: float = 1.0):
-    """One decode step (plan inside the attention kernel, attention, merge);
-    `plan` from hpc_decode_plan_create, `seq_lens` an int32 CUDA tensor."""
+    """One decode step planned on the device (one step-kernel launch for one
+    query token per sequence and at most 3072 sequences); `plan` from
+    hpc_decode_plan_create, `seq_lens` an int32 CUDA tensor."""
     lib = load_library()
     tq, tk, tv = make_tensor(q), make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
     tb, ts, to = make_tensor(block_table), make_tensor(seq_lens), make_tensor(out)
@@ -378,6 +381,22 @@ def hpc_decode_step(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_
     ref = lambda d: ctypes.byref(d) if d is not None else None
     _check(lib.hpc_decode_step(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), plan.handle,
                                int(num_sms), ref(to), ref(tl), _stream_ptr(stream)))
+
+
+def hpc_decode_step_host(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, num_sms: int,
+                         out, lse=None, stream=None, k_scale: float = 1.0, v_scale: float = 1.0):
+    """hpc_decode_step with q, block_table, seq_lens, out and lse in host
+    memory (contiguous CPU tensors; pinned ones make the copies
+    asynchronous): the library enqueues the copies in, the step and the
+    copies out on `stream`. The caches are CUDA tensors. `out` / `lse` hold
+    the result once the stream has passed the copies out."""
+    lib = load_library()
+    tq, tk, tv = make_tensor(q), make_tensor(k_cache, k_scale), make_tensor(v_cache, v_scale)
+    tb, ts, to = make_tensor(block_table), make_tensor(seq_lens), make_tensor(out)
+    tl = make_tensor(lse)
+    ref = lambda d: ctypes.byref(d) if d is not None else None
+    _check(lib.hpc_decode_step_host(ref(tq), ref(tk), ref(tv), ref(tb), ref(ts), plan.handle,
+                                    int(num_sms), ref(to), ref(tl), _stream_ptr(stream)))
 
 
 def hpc_decode_attn(q, k_cache, v_cache, block_table, seq_lens, plan: Plan, out, lse=None,

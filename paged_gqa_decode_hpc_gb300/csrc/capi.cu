@@ -100,6 +100,7 @@ void free_plan(hpc_plan_s* pl) {
   if (pl->d_err) cudaFree(pl->d_err);
   if (pl->d_ws) cudaFree(pl->d_ws);
   if (pl->d_step) cudaFree(pl->d_step);
+  if (pl->d_stage) cudaFree(pl->d_stage);
   if (pl->h_pinned) cudaFreeHost(pl->h_pinned);
   if (pl->copy_done) cudaEventDestroy(pl->copy_done);
   delete pl;
@@ -900,6 +901,70 @@ hpc_status hpc_decode_step(const hpc_tensor* q, const hpc_tensor* k_cache,
   plan->host_num_segs = -1;
   return attn_impl(q, k_cache, v_cache, block_table, seq_lens, plan, out, lse, -1.0f, stream,
                    num_sms, false);
+}
+
+// A host tensor of the step's batch: present, 1 to 4 dims, dense (outermost
+// first), so one copy moves it; its size in bytes.
+static bool host_dense(const hpc_tensor* t, size_t* bytes) {
+  if (!t || !t->data || t->ndim < 1 || t->ndim > 4) return false;
+  const size_t eb = t->dtype == HPC_BF16 ? 2 : t->dtype == HPC_FP8_E4M3 ? 1 : 4;
+  int64_t n = 1;
+  for (int i = t->ndim - 1; i >= 0; --i) {
+    if (t->shape[i] < 0) return false;
+    if (t->shape[i] > 1 && t->stride[i] != n) return false;
+    n *= t->shape[i];
+  }
+  *bytes = (size_t)n * eb;
+  return true;
+}
+
+hpc_status hpc_decode_step_host(const hpc_tensor* q, const hpc_tensor* k_cache,
+                                const hpc_tensor* v_cache, const hpc_tensor* block_table,
+                                const hpc_tensor* seq_lens, hpc_plan_t plan, int32_t num_sms,
+                                hpc_tensor* out, hpc_tensor* lse, void* stream) {
+  if (!plan) return fail(HPC_ERR_INVALID_ARG, "plan is null");
+  const hpc_tensor* host[5] = {q, block_table, seq_lens, out, lse};
+  const char* names[5] = {"q", "block_table", "seq_lens", "out", "lse"};
+  size_t bytes[5] = {0, 0, 0, 0, 0}, off[6] = {0, 0, 0, 0, 0, 0};
+  for (int i = 0; i < 5; ++i) {
+    if (i == 4 && !lse) {
+      off[i + 1] = off[i];
+      continue;
+    }
+    if (!host_dense(host[i], &bytes[i]))
+      return fail(HPC_ERR_INVALID_ARG,
+                  std::string(names[i]) + " must be a dense host tensor of 1 to 4 dims");
+    off[i + 1] = off[i] + (bytes[i] + 255) / 256 * 256;
+  }
+  const size_t need = off[5] > 256 ? off[5] : 256;
+  if (plan->stage_bytes < need) {
+    if (plan->d_stage) {
+      HPC_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));  // the old area's last use
+      cudaFree(plan->d_stage);
+      plan->d_stage = nullptr;
+      plan->stage_bytes = 0;
+    }
+    HPC_CUDA_TRY(cudaMalloc(&plan->d_stage, need));
+    plan->stage_bytes = need;
+  }
+  hpc_tensor dev[5];
+  for (int i = 0; i < 5; ++i) {
+    if (!host[i]) continue;
+    dev[i] = *host[i];
+    dev[i].data = static_cast<uint8_t*>(plan->d_stage) + off[i];
+  }
+  const cudaStream_t s = (cudaStream_t)stream;
+  for (int i = 0; i < 3; ++i)  // q, block table, lengths up
+    if (bytes[i]) HPC_CUDA_TRY(cudaMemcpyAsync(dev[i].data, host[i]->data, bytes[i],
+                                               cudaMemcpyHostToDevice, s));
+  const hpc_status st = hpc_decode_step(&dev[0], k_cache, v_cache, &dev[1], &dev[2], plan, num_sms,
+                                        &dev[3], lse ? &dev[4] : nullptr, stream);
+  if (st != HPC_OK) return st;
+  for (int i = 3; i < 5; ++i)  // out and lse down
+    if (host[i] && bytes[i])
+      HPC_CUDA_TRY(cudaMemcpyAsync(host[i]->data, dev[i].data, bytes[i], cudaMemcpyDeviceToHost,
+                                   s));
+  return HPC_OK;
 }
 
 hpc_status hpc_decode_tc_min_q_len(int32_t q_len, int32_t* previous) {

@@ -66,6 +66,9 @@ struct hpc_plan_s {
   // zero by every step; sized for step_kv_heads KV heads.
   int32_t* d_step = nullptr;
   int32_t step_kv_heads = 0;
+  // hpc_decode_step_host: device staging for the step's host-side buffers
+  void* d_stage = nullptr;
+  size_t stage_bytes = 0;
   int64_t ws_floats = 0;         // floats allocated at d_ws
 };
 

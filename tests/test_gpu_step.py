@@ -262,3 +262,37 @@ def test_step_full_size_configs(name):
     out, lse, words, err = run_step(w)
     assert err == 0
     assert_parity(out, lse, ref_out, ref_lse, label=f"step {name}")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_step_host_entry_matches_the_device_step(fp8):
+    # hpc_decode_step_host: the batch and the results in pinned host memory,
+    # copied by the library around the same step -- the same bits as
+    # hpc_decode_step, and the oracle's values; a larger batch regrows the
+    # plan's staging area, a smaller one reuses it
+    sms = hpc.hpc_device_sm_count()
+    plan = hpc.hpc_decode_plan_create(16, sms, 64)
+    for lens in ([300, 5, 0, 2000, 64], [1, 63, 64, 65, 127, 129, 700, 3001, 40, 9000], [77]):
+        w = W.make_workload(_cfg(64, 8, fp8), lengths=lens, seed=45)
+        d = device_workload(w)
+        out = torch.empty(w.q.shape, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(w.q.shape[:2], dtype=torch.float32, device="cuda")
+        hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, sms, out, lse,
+                            k_scale=w.k_scale, v_scale=w.v_scale)
+        pin = lambda t: t.clone().pin_memory()
+        q_h, bt_h, sl_h = pin(w.q), pin(w.block_table), pin(w.seq_lens)
+        out_h = torch.full(w.q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.full(w.q.shape[:2], float("nan"), dtype=torch.float32).pin_memory()
+        hpc.hpc_decode_step_host(q_h, d["k"], d["v"], bt_h, sl_h, plan, sms, out_h, lse_h,
+                                 k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())
+        ref_out, ref_lse = oracle.decode_workload(w)
+        assert_parity(out_h.double().numpy(), lse_h.double().numpy(), ref_out, ref_lse,
+                      label=f"host entry {lens[:3]}")
+    # a strided (non-dense) host tensor is refused before any copy
+    with pytest.raises(hpc.HpcError) as e:
+        hpc.hpc_decode_step_host(q_h[:, ::2], d["k"], d["v"], bt_h, sl_h, plan, sms,
+                                 out_h[:, ::2], lse_h)
+    assert e.value.status == hpc.HPC_ERR_INVALID_ARG
+    plan.destroy()
