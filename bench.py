@@ -122,10 +122,20 @@ def extend_flops(lens, qn, num_q_heads):
     return 4 * 128 * num_q_heads * vis
 
 
+def _code_only(text):
+    """C / C++ source without its comments and with whitespace runs
+    collapsed: what the compiler sees of it (string literals in this
+    source hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest():
-    """Digest of the timed kernel's source: step_kernel.cu and every file it
-    includes from the package's csrc/ or include/ directories,
-    transitively."""
+    """Digest of the timed kernel's code: step_kernel.cu and every file it
+    includes from the package's csrc/ or include/ directories, transitively,
+    each without its comments (a comment edit does not make a profile
+    stale; any code change does)."""
     dirs = [os.path.join(ROOT, "paged_gqa_decode_hpc_gb300", "csrc"), os.path.join(ROOT, "include")]
     h = hashlib.sha256()
     seen, todo = set(), ["step_kernel.cu"]
@@ -140,7 +150,7 @@ def kernel_source_digest():
         seen.add(name)
         with open(path, "rb") as f:
             data = f.read()
-        h.update(name.encode() + b"\0" + data)
+        h.update(name.encode() + b"\0" + _code_only(data.decode("utf-8", "replace")).encode())
         todo += re.findall(r'^\s*#\s*include\s+"([^"]+)"', data.decode("utf-8", "replace"), re.M)
     return h.hexdigest()[:16]
 

@@ -11,15 +11,16 @@
 // holds whole (sequence, KV head) pairs where it can:
 //  * sequence b has n_b * H_kv units, unit u being tile u % n_b of KV head
 //    u / n_b; units are flattened in sequence order (T in all);
-//  * the first S = T - floor(T / 8) units are split into P = min(G, S)
-//    balanced contiguous parts (part p = [floor(pS/P), floor((p+1)S/P))),
-//    one per CTA; the rest is a pool of chunks of C units that CTAs take with
+//  * the first S = T - floor(T / 8) units are split into P = min(G,
+//    ceil(S / 8)) balanced contiguous parts (part p = [floor(pS/P),
+//    floor((p+1)S/P))), one per CTA; the rest is a pool of chunks of
+//    C = max(8, ceil(S / (12 P)), ceil(W / (4 G))) units that CTAs take with
 //    an atomic counter as they run out of work, so SMs that stream faster
 //    than others take more of it;
 //  * a piece is an owner's range (a part or a chunk) intersected with one
-//    pair; the 8 consumer warps share a piece's tiles round-robin, then
-//    combine their 8 states in shared memory (warp w combines dims
-//    [16w, 16w + 16) of the 8 query heads);
+//    pair; the 8 consumer warps share a piece's tiles round-robin, then each
+//    deposits its state (o = acc / l as 16-bit pairs, (m, l) in fp32) in
+//    shared memory and goes on, and an epilogue warp combines the 8 states;
 //  * a pair held by one piece is final and written as bf16 out + lse; the k
 //    pieces of a split pair each leave a partial state in slot 2*owner (the
 //    owner's first piece) or 2*owner + 1 (its last) and count themselves in

@@ -81,3 +81,19 @@ def test_kernel_source_digest_follows_includes(tmp_path, monkeypatch):
     assert d1 != d0
     (inc / "api.h").write_text("abi v2\n")
     assert bench.kernel_source_digest() != d1
+
+
+def test_kernel_source_digest_ignores_comments_only(tmp_path, monkeypatch):
+    """A comment or whitespace edit keeps the digest (the compiled kernel is
+    the same); any code edit changes it."""
+    csrc = tmp_path / "paged_gqa_decode_hpc_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
+    k = csrc / "step_kernel.cu"
+    k.write_text('// v1 of a comment\nint f(int x) { /* block */ return x + 1; }\n')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d0 = bench.kernel_source_digest()
+    k.write_text('// a different comment\n\nint f(int x) {  /* other\n block */ return x + 1; }\n')
+    assert bench.kernel_source_digest() == d0
+    k.write_text('// v1 of a comment\nint f(int x) { /* block */ return x + 2; }\n')
+    assert bench.kernel_source_digest() != d0
