@@ -22,13 +22,8 @@ formula; this oracle takes the plainest reading:
 Step plan -- the work list of one decode step with one query token, as the
 step call runs it. The same partition rule is applied to finer units, ordered
 so that a part's range holds whole (sequence, KV head) pairs where it can:
-  * a unit is unit_tiles consecutive 64-token tiles of one KV head (1 for a
-    bf16 cache; 2 for an e4m3 cache, whose tiles carry half the bytes, so a
-    unit moves as many bytes as a bf16 one); sequence b has
-    n_b = ceil(tiles_b / unit_tiles) units per KV head, the last one holding
-    the remaining tile(s);
-  * sequence b has n_b * H_kv units; unit u of the sequence is unit u % n_b
-    of KV head u // n_b (head-major: a pair's units are adjacent);
+  * sequence b has n_b * H_kv units; unit u of the sequence is tile u % n_b
+    of KV head u // n_b (head-major: a pair's tiles are adjacent);
   * units are flattened in sequence order; T = sum_b n_b * H_kv;
   * the last W = floor(T / 8) units form a pool, S = T - W units are static;
   * P = min(num_sms, ceil(S / 8)) static parts: no more parts than it takes
@@ -165,7 +160,7 @@ class Piece(NamedTuple):
     owner: int       # static part p < P, or P + chunk index
     seq: int
     head: int        # KV head
-    tile_begin: int  # first unit of the pair (tiles with unit_tiles = 1)
+    tile_begin: int
     tile_end: int
     whole: bool      # covers every tile of its (sequence, head) pair
     slot: int        # partial-state slot; -1 for a whole pair
@@ -180,15 +175,12 @@ class StepPlan(NamedTuple):
     owner_start: List[int]   # [P + chunks + 1] first unit of every owner, then T
     pieces: List[Piece]      # by owner, then in unit order
     pair_pieces: dict        # (seq, head) -> number of pieces (pairs with tiles only)
-    unit_tiles: int = 1      # 64-token tiles per unit
 
 
-def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int,
-              unit_tiles: int = 1) -> StepPlan:
-    if num_sms <= 0 or num_kv_heads <= 0 or unit_tiles <= 0 or any(L < 0 for L in seq_lens):
-        raise ValueError("num_sms, num_kv_heads and unit_tiles must be positive, "
-                         "lengths non-negative")
-    n = [-(-c // unit_tiles) for c in tile_counts(seq_lens)]
+def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int) -> StepPlan:
+    if num_sms <= 0 or num_kv_heads <= 0 or any(L < 0 for L in seq_lens):
+        raise ValueError("num_sms and num_kv_heads must be positive, lengths non-negative")
+    n = tile_counts(seq_lens)
     H = num_kv_heads
     T = sum(c * H for c in n)
     W = T // POOL_DIV
@@ -222,4 +214,4 @@ def step_plan(seq_lens: List[int], num_sms: int, num_kv_heads: int,
     pair_pieces: dict = {}
     for pc in pieces:
         pair_pieces[(pc.seq, pc.head)] = pair_pieces.get((pc.seq, pc.head), 0) + 1
-    return StepPlan(T, S, P, C, chunks, owner_start, pieces, pair_pieces, unit_tiles)
+    return StepPlan(T, S, P, C, chunks, owner_start, pieces, pair_pieces)

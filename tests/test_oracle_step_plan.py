@@ -25,8 +25,8 @@ def _lengths(case):
     return out
 
 
-def check_step(lengths, num_sms, H, sp, unit_tiles=1):
-    n = [-(-((L + 63) // 64) // unit_tiles) for L in lengths]
+def check_step(lengths, num_sms, H, sp):
+    n = [(L + 63) // 64 for L in lengths]
     T = H * sum(n)
     assert sp.num_units == T
     W = T - sp.static_units
@@ -173,38 +173,3 @@ def test_skewed_pool_chunks_are_quarter_pairs():
     assert all(pc.tile_end - pc.tile_begin == 16 and not pc.whole for pc in pool)
     pairs = {(pc.seq, pc.head) for pc in pool}
     assert len(pairs) == 63 and all(sp.pair_pieces[k] == 4 for k in pairs)
-
-
-def test_two_tile_units_reduce_to_single_tile_units():
-    """With unit_tiles = 2 a sequence of c tiles has ceil(c / 2) units per KV
-    head; the plan is exactly the one-tile plan of a sequence with that many
-    tiles (lengths 64 * ceil(c / 2)): same parts, pool, chunks and pieces."""
-    rng = __import__("random").Random(11)
-    for _ in range(80):
-        lens = [rng.choice([0, 1, 64, 65, 127, 128, 129, rng.randint(1, 9000)])
-                for _ in range(rng.randint(1, 20))]
-        H = rng.choice([1, 2, 4, 8])
-        sms = rng.choice([1, 3, 64, 152])
-        two = plan_ref.step_plan(lens, sms, H, unit_tiles=2)
-        halved = [64 * (-(-((L + 63) // 64) // 2)) for L in lens]
-        one = plan_ref.step_plan(halved, sms, H)
-        assert two.unit_tiles == 2 and one.unit_tiles == 1
-        assert (two.num_units, two.static_units, two.num_parts, two.chunk_units,
-                two.num_chunks, two.owner_start, two.pieces, two.pair_pieces) == \
-            (one.num_units, one.static_units, one.num_parts, one.chunk_units,
-             one.num_chunks, one.owner_start, one.pieces, one.pair_pieces)
-        check_step(lens, sms, H, two, unit_tiles=2)
-
-
-def test_skewed_fp8_shape_with_two_tile_units():
-    """Worked by hand for the skewed batch with an e4m3 cache (two tiles per
-    unit) on 152 CTAs: units per KV head 1024 (131072 tokens) and 32 (4096);
-    T = 8 * (1024 + 31 * 32) = 16128; W = 2016; S = 14112; P = 152;
-    C = max(8, ceil(14112 / 1824) = 8, ceil(2016 / 608) = 4) = 8; 252 chunks,
-    each a quarter of one of the last 63 (sequence, KV head) pairs of 32
-    units (S = 441 * 32)."""
-    sp = plan_ref.step_plan([131072] + [4096] * 31, 152, 8, unit_tiles=2)
-    assert (sp.num_units, sp.static_units, sp.num_parts, sp.chunk_units, sp.num_chunks) == \
-        (16128, 14112, 152, 8, 252)
-    pool = [pc for pc in sp.pieces if pc.owner >= sp.num_parts]
-    assert len(pool) == 252 and all(pc.tile_end - pc.tile_begin == 8 for pc in pool)
