@@ -280,7 +280,11 @@ hpc_status hpc_decode_attn(const hpc_tensor* q, const hpc_tensor* k_cache,
  * Allocates nothing; may be captured in a CUDA graph after a first call
  * outside the capture.
  *   q, k_cache, v_cache, block_table, out, lse: as hpc_decode_attn
- *   seq_lens  device int32 [B], contiguous
+ *   seq_lens  device int32 [B], contiguous; on the one-token route a negative
+ *             length, a sequence of more than INT32_MAX / 352 (tile, KV head)
+ *             units, or more than INT32_MAX units in all set
+ *             HPC_DEVCHK_BAD_LENGTH and the step writes out = 0, lse = -inf
+ *             for every sequence
  *   plan      from hpc_decode_plan_create with max_seqs >= B
  *   num_sms   CTAs of the persistent grid, <= the plan's num_sms
  */

@@ -310,8 +310,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
     int32_t n = 0;
     if (b < B) {
       const int32_t len = p.seq_lens[b];
-      if (len < 0) *s_bad = 1;
-      n = len > 0 ? (int32_t)((len + kBlockTokens - 1) / kBlockTokens) * H : 0;
+      // a sequence of more units than INT32_MAX / kSThreads is reported, so
+      // that no partial sum of a scan pass (kSThreads sequences) wraps
+      const int64_t units = len > 0 ? ((int64_t)len + kBlockTokens - 1) / kBlockTokens * H : 0;
+      if (len < 0 || units > (int64_t)(INT32_MAX / kSThreads)) *s_bad = 1;
+      else n = (int32_t)units;
     }
     int32_t tot;
     const int32_t incl = cta_inclusive_scan(n, warp_tot, &tot);

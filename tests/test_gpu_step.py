@@ -183,6 +183,14 @@ def test_step_negative_length_sets_check():
     out, lse, words, err = run_step(w, d=d)
     assert err & hpc.HPC_DEVCHK_BAD_LENGTH
     assert words[3] == 0 and words[5] == 0  # empty plan
+    # a length whose (tile, KV head) units could wrap the plan's 32-bit scan
+    # (2^30 tokens x 8 KV heads) is refused the same way, before any copy:
+    # every output row is 0 and every lse -inf
+    d["sl"][1] = 1 << 30
+    out, lse, words, err = run_step(w, d=d)
+    assert err & hpc.HPC_DEVCHK_BAD_LENGTH
+    assert words[3] == 0 and words[5] == 0
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
 
 
 def test_step_reuses_one_plan_across_batches_and_graph_capture():
