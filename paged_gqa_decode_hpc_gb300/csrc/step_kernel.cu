@@ -27,6 +27,9 @@
 //    the pair's arrival counter; the CTA that brings the counter to k merges
 //    the k states (M = max m_i, l = sum l_i 2^(m_i - M), out = sum o_i
 //    2^(m_i - M) / l) and resets the counter to zero. No merge kernel runs.
+//    An owner's pieces run split ones first (its first piece, then its last
+//    when that pair continues past the range), whole pairs last, so merges
+//    overlap the streaming instead of following it;
 //  * every CTA plans the step itself from the device lengths (a prefix scan
 //    in shared memory), and CTAs with no static part start on the pool.
 //
@@ -404,77 +407,125 @@ __global__ void __launch_bounds__(kSThreads, 1)
       ask();
       owner = resolve();
     }
+    // the sequence holding unit x (cu[b] <= x < cu[b + 1])
+    auto seq_at = [&](uint32_t x) -> int {
+      int l0 = 0, h0 = B;  // last b with cu[b] <= x, then past empty sequences
+      while (h0 - l0 > 1) {
+        const int mid = (l0 + h0) >> 1;
+        if ((uint32_t)cu[mid] <= x) l0 = mid; else h0 = mid;
+      }
+      while ((uint32_t)cu[l0 + 1] <= x) ++l0;
+      return l0;
+    };
     while (owner >= 0) {
       const uint32_t lo = M.start(owner), hi = M.end(owner);
       int npieces = 0;
-      int b;
+      // The owner's unit ranges, walked in this order: its first piece; then
+      // its last piece when that is the head of a pair continuing past hi;
+      // then the whole pairs between them. Both sides of a part boundary are
+      // then computed early, so the arrival counts and merges of the pairs
+      // that boundaries split overlap the streaming of the rest, and a part
+      // ends on a whole pair (a final write). Pieces, slots and every result
+      // bit are those of the unit order.
+      uint32_t ra = lo, rb = hi;         // the range being walked
+      uint32_t rest_a = hi, rest_b = hi;  // whole pairs left for after it
+      bool first = false;                 // walking the first of several pieces
+      int b = seq_at(lo);
       {
-        int l0 = 0, h0 = B;  // last b with cu[b] <= lo
-        while (h0 - l0 > 1) {
-          const int mid = (l0 + h0) >> 1;
-          if ((uint32_t)cu[mid] <= lo) l0 = mid; else h0 = mid;
+        const uint32_t nb0 = (uint32_t)(cu[b + 1] - cu[b]) / (uint32_t)H;
+        const uint32_t e0 = (uint32_t)cu[b] + ((lo - (uint32_t)cu[b]) / nb0 + 1) * nb0;
+        if (e0 < hi) {
+          rb = e0;
+          first = true;
         }
-        b = l0;
       }
-      for (uint32_t u = lo; u < hi;) {
-        while ((uint32_t)cu[b + 1] <= u) ++b;
-        const uint32_t nb = (uint32_t)(cu[b + 1] - cu[b]) / (uint32_t)H;
-        const uint32_t rel = u - (uint32_t)cu[b];
-        const uint32_t hu = rel / nb;
-        const int h = (int)hu, t0 = (int)(rel - hu * nb);
-        const uint32_t pair_lo = (uint32_t)cu[b] + hu * nb, pair_hi = pair_lo + nb;
-        const uint32_t e = hi < pair_hi ? hi : pair_hi;
-        const int t1 = t0 + (int)(e - u);
-        const bool whole = t0 == 0 && t1 == (int)nb;
-        const int slot = whole ? -1 : (u == lo ? 2 * owner : 2 * owner + 1);
-        const int k = whole ? 1 : (int)(M.owner_of(pair_hi - 1) - M.owner_of(pair_lo) + 1);
-        publish(b, h, t0, t1, (whole ? kFlagWhole : 0) | (k << 8), slot);
-        ++npieces;
-        const int32_t* btrow = p.block_table + (int64_t)b * p.bt_sb;
-        const int n = t1 - t0;
-        const int c1 = p.kv_swap ? h : 0, c2 = p.kv_swap ? 0 : h;
-        for (int i0 = 0; i0 < n; i0 += 32) {
-          const int i = i0 + lane;
-          int blk = p.num_blocks;  // out of range: TMA fills zeros
-          if (i < n) {
-            const int t = t0 + i;
-            if (t < p.max_blocks) {
-              const int v = __ldg(btrow + t);
-              if (v >= 0 && v < p.num_blocks) blk = v;
-              else atomicOr(p.err, HPC_DEVCHK_BAD_BLOCK);
-            } else {
-              atomicOr(p.err, HPC_DEVCHK_TABLE_TOO_SHORT);
+      uint32_t left = hi - lo;  // units of this owner from the current one on
+      for (;;) {
+        for (uint32_t u = ra; u < rb;) {
+          while ((uint32_t)cu[b + 1] <= u) ++b;
+          const uint32_t nb = (uint32_t)(cu[b + 1] - cu[b]) / (uint32_t)H;
+          const uint32_t rel = u - (uint32_t)cu[b];
+          const uint32_t hu = rel / nb;
+          const int h = (int)hu, t0 = (int)(rel - hu * nb);
+          const uint32_t pair_lo = (uint32_t)cu[b] + hu * nb, pair_hi = pair_lo + nb;
+          const uint32_t e = rb < pair_hi ? rb : pair_hi;
+          const int t1 = t0 + (int)(e - u);
+          const bool whole = t0 == 0 && t1 == (int)nb;
+          const int slot = whole ? -1 : (u == lo ? 2 * owner : 2 * owner + 1);
+          const int k = whole ? 1 : (int)(M.owner_of(pair_hi - 1) - M.owner_of(pair_lo) + 1);
+          publish(b, h, t0, t1, (whole ? kFlagWhole : 0) | (k << 8), slot);
+          ++npieces;
+          const int32_t* btrow = p.block_table + (int64_t)b * p.bt_sb;
+          const int n = t1 - t0;
+          const int c1 = p.kv_swap ? h : 0, c2 = p.kv_swap ? 0 : h;
+          for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            int blk = p.num_blocks;  // out of range: TMA fills zeros
+            if (i < n) {
+              const int t = t0 + i;
+              if (t < p.max_blocks) {
+                const int v = __ldg(btrow + t);
+                if (v >= 0 && v < p.num_blocks) blk = v;
+                else atomicOr(p.err, HPC_DEVCHK_BAD_BLOCK);
+              } else {
+                atomicOr(p.err, HPC_DEVCHK_TABLE_TOO_SHORT);
+              }
+            }
+            const int cnt = n - i0 < 32 ? n - i0 : 32;
+            for (int ii = 0; ii < cnt; ++ii, ++g, --left) {
+              const int bk = __shfl_sync(0xffffffffu, blk, ii);
+              if (!asked && left <= (uint32_t)kClaimAhead) ask();
+              if (lane != 0 || stop) continue;
+              const uint32_t slot_r = g % STAGES;
+              if (!wait_phase(bar_empty + 8 * slot_r, ((g / STAGES) & 1u) ^ 1u, abort_flag, p.err,
+                              p.timeout_ns)) {
+                stop = true;
+                continue;
+              }
+              const uint32_t fb = bar_full + 8 * slot_r;
+              const uint32_t dk = smem_base + slot_r * kStage;
+              const uint32_t dv = dk + kTile;
+              mbar_arrive_expect_tx(fb, kStage);
+              if constexpr (FP8) {
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
+              } else {
+                tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dk + 8192, &tmk, fb, 64, c1, c2, bk, policy);
+                tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
+                tma_load_4d(dv + 8192, &tmv, fb, 64, c1, c2, bk, policy);
+              }
+              st_release_shared(issued_word + 4 * slot_r, g);
+              issued = g + 1;
             }
           }
-          const int cnt = n - i0 < 32 ? n - i0 : 32;
-          for (int ii = 0; ii < cnt; ++ii, ++g) {
-            const int bk = __shfl_sync(0xffffffffu, blk, ii);
-            if (!asked && hi - (u + (uint32_t)(i0 + ii)) <= (uint32_t)kClaimAhead) ask();
-            if (lane != 0 || stop) continue;
-            const uint32_t slot_r = g % STAGES;
-            if (!wait_phase(bar_empty + 8 * slot_r, ((g / STAGES) & 1u) ^ 1u, abort_flag, p.err,
-                            p.timeout_ns)) {
-              stop = true;
-              continue;
-            }
-            const uint32_t fb = bar_full + 8 * slot_r;
-            const uint32_t dk = smem_base + slot_r * kStage;
-            const uint32_t dv = dk + kTile;
-            mbar_arrive_expect_tx(fb, kStage);
-            if constexpr (FP8) {
-              tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
-              tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
-            } else {
-              tma_load_4d(dk, &tmk, fb, 0, c1, c2, bk, policy);
-              tma_load_4d(dk + 8192, &tmk, fb, 64, c1, c2, bk, policy);
-              tma_load_4d(dv, &tmv, fb, 0, c1, c2, bk, policy);
-              tma_load_4d(dv + 8192, &tmv, fb, 64, c1, c2, bk, policy);
-            }
-            st_release_shared(issued_word + 4 * slot_r, g);
-            issued = g + 1;
-          }
+          u = e;
         }
-        u = e;
+        if (first) {  // then the last piece, if split, ahead of the whole pairs
+          first = false;
+          const uint32_t e0 = rb;
+          const int b1 = seq_at(hi - 1);
+          const uint32_t nb1 = (uint32_t)(cu[b1 + 1] - cu[b1]) / (uint32_t)H;
+          const uint32_t s1 = (uint32_t)cu[b1] + ((hi - 1 - (uint32_t)cu[b1]) / nb1) * nb1;
+          if (s1 + nb1 > hi && s1 > e0) {
+            rest_a = e0;
+            rest_b = s1;
+            ra = s1;
+            b = b1;
+          } else {
+            ra = e0;
+          }
+          rb = hi;
+          continue;
+        }
+        if (rest_a < rest_b) {
+          ra = rest_a;
+          rb = rest_b;
+          rest_a = rest_b;
+          b = seq_at(ra);
+          continue;
+        }
+        break;
       }
       if (lane == 0 && p.rec) {
         int32_t* r = p.rec + 4 * owner;
