@@ -138,6 +138,40 @@ def test_step_bit_identical_under_block_permutation(fp8):
     assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_step_token_major_cache_layout(fp8):
+    """A [blocks][64][H_kv][128] (token-major) cache passed as a
+    [blocks][H_kv][64][128] view: the step kernel's copies take the other
+    coordinate order and give the same bits as the head-major cache."""
+    w = W.make_workload(_cfg(64, 8, fp8), lengths=[300, 64, 1000, 0, 4097], seed=54)
+    out, lse, _, err = run_step(w, num_sms=23)
+    assert err == 0
+    d = device_workload(w)
+    for k in ("k", "v"):
+        d[k] = d[k].permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+    assert d["k"].stride(1) == 128 and d["k"].stride(2) == 8 * 128
+    out2, lse2, _, err2 = run_step(w, d=d, num_sms=23)
+    assert err2 == 0
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+    ref_out, ref_lse = oracle.decode_workload(w)
+    assert_parity(out2, lse2, ref_out, ref_lse, label="step, token-major cache")
+
+
+def test_step_without_lse():
+    """lse is optional: the output bits are those of a step that writes it."""
+    w = W.make_workload(_cfg(64, 8), lengths=[2000, 7, 640, 0, 129], seed=55)
+    out, _, _, err = run_step(w, num_sms=11)
+    assert err == 0
+    d = device_workload(w)
+    plan = hpc.hpc_decode_plan_create(8, hpc.hpc_device_sm_count(), 64)
+    o2 = torch.full((5, 64, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    hpc.hpc_decode_step(d["q"], d["k"], d["v"], d["bt"], d["sl"], plan, 11, o2, None)
+    torch.cuda.synchronize()
+    assert hpc.hpc_decode_plan_status(plan) == 0
+    plan.destroy()
+    assert np.array_equal(out, o2.double().cpu().numpy())
+
+
 def test_step_records_count_every_run():
     lens = [4096] * 6 + [70]
     w = W.make_workload(_cfg(64, 8), lengths=lens, seed=54)
@@ -262,9 +296,9 @@ def test_unit_plan_merges_with_partial_head_segments(sms):
 
 @pytest.mark.parametrize("name", ["tiny", "uniform", "skewed_fp8", "random_mixed"])
 def test_step_full_size_configs(name):
-    # the launch configuration bench.py times (hpc_decode_step: the plan built
-    # in the attention kernel's prologue, then the merge), at each config's
-    # full size, element by element against the fp64 oracle
+    # the launch configuration bench.py times (hpc_decode_step: one launch of
+    # the step kernel, which plans, computes and merges the step), at each
+    # config's full size, element by element against the fp64 oracle
     w = W.make_workload(name)
     ref_out, ref_lse = oracle.decode_workload(w)
     out, lse, words, err = run_step(w)
