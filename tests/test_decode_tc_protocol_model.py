@@ -2,14 +2,16 @@
 synchronisation protocol (csrc/decode_tc_kernel.cu), checked under thousands
 of random interleavings. One CTA walks a list of segments (a sequence's tile
 range each); its roles (TMA producer, e4m3 converters for FP8 caches, the
-MMA warp, the softmax warpgroup, the in-order tensor pipe) run as step-wise
-processes; mbarriers have their hardware semantics (phases, arrival counts,
+MMA warp, the softmax warps -- one holding query rows and one holding only
+padding rows, which keeps the barrier counts without work -- and the
+in-order tensor pipe) run as step-wise processes; mbarriers have their hardware semantics (phases, arrival counts,
 waits on a phase PARITY only); a commit fires once every earlier operation
 of the issuing warp has completed.
 
 Checked, across segment boundaries: no wait passes on a stale phase, no
 buffer is overwritten before its reader is done (the two Q slots, K/V and
-e4m3 ring slots, the single S buffer, the two P buffers), with an FP8
+e4m3 ring slots, the single S buffer, the two P buffers), no P V reads a P
+buffer that its softmax warps have not all written, with an FP8
 cache no S MMA reads a Q slot before the softmax warps converted it to f16
 for its segment and no Q slot is reloaded while it is being converted, the
 first P V of a
@@ -24,6 +26,7 @@ import random
 import pytest
 
 WAIT = "wait"  # yielded by a role that is spinning on a barrier (not progress)
+NSM = 2        # softmax roles: 0 holds query rows, 1 only padding rows
 
 
 class Barrier:
@@ -55,15 +58,15 @@ class Model:
         self.q_full = [B(f"q_full{i}", 1) for i in range(2)]
         self.q_empty = [B(f"q_empty{i}", 1) for i in range(2)]
         # FP8: the softmax warps convert a segment's Q slot to f16 in place
-        self.q_ready = [B(f"q_ready{i}", 1) for i in range(2)]
+        self.q_ready = [B(f"q_ready{i}", NSM) for i in range(2)]
         self.q_conv = [None, None]          # segment whose Q a slot holds as f16
         self.q_converting = [False, False]
         self.kv_full = [B(f"kv_full{s}", 1) for s in range(stages)]
         self.kv_empty = [B(f"kv_empty{s}", 1) for s in range(stages)]
         self.kv8_full = [B(f"kv8_full{s}", 1) for s in range(stages8)]
         self.kv8_empty = [B(f"kv8_empty{s}", 1) for s in range(stages8)]
-        self.s_full, self.s_free = B("s_full", 1), B("s_free", 1)
-        self.p_full = [B(f"p_full{i}", 1) for i in range(2)]
+        self.s_full, self.s_free = B("s_full", 1), B("s_free", NSM)
+        self.p_full = [B(f"p_full{i}", NSM) for i in range(2)]
         self.pv_done = [B(f"pv_done{i}", 1) for i in range(2)]
         # tile g of the CTA's stream belongs to segment seg_of[g]
         self.seg_of = [k for k, n in enumerate(segs) for _ in range(n)]
@@ -76,7 +79,7 @@ class Model:
         self.slot8 = [None] * stages8
         self.readers = {}                  # tile -> pending MMA reads of its bf16 slot
         self.conv_reading = set()
-        self.S_buf, self.S_read = None, True
+        self.S_buf, self.S_read_by = None, set(range(NSM))  # S's tile, roles that copied it
         self.P_buf = [None, None]
         self.pv_pending = set()
         self.pv_reading_P = [None, None]
@@ -198,28 +201,35 @@ class Model:
                 yield from m.issue_pv(G + j, k, j > 0)
             G += n
 
-    def softmax(self):
+    def softmax(self, role=0):
         m = self
+        live = role == 0
         G = 0
         for k, n in enumerate(m.segs):
             if m.fp8:  # convert this segment's Q rows once they landed
                 while not m.q_full[k & 1].ready(k >> 1):
                     yield WAIT
                 assert m.q_slot[k & 1] == k, "converted a Q slot holding another segment"
-                m.q_converting[k & 1] = True
-                for _ in range(m.rng.randint(1, 5)):
-                    yield
-                m.q_converting[k & 1] = False
-                m.q_conv[k & 1] = k
+                if live:
+                    m.q_converting[k & 1] = True
+                    for _ in range(m.rng.randint(1, 5)):
+                        yield
+                    m.q_converting[k & 1] = False
+                    m.q_conv[k & 1] = k
                 m.q_ready[k & 1].arrive()
                 yield
             for j in range(n):
                 g = G + j
                 while not m.s_full.ready(g):
                     yield WAIT
-                assert m.S_buf == g and not m.S_read, "softmax read a stale S"
-                m.S_read = True
+                assert m.S_buf == g and role not in m.S_read_by, "softmax read a stale S"
+                m.S_read_by.add(role)
                 m.s_free.arrive()
+                if not live:  # padding rows: the barrier counts only
+                    yield
+                    m.p_full[g & 1].arrive()
+                    yield
+                    continue
                 for _ in range(m.rng.randint(1, 8)):
                     yield
                 if j > 0 and m.rng.random() < m.rescale_p:  # the row maximum moved
@@ -233,6 +243,9 @@ class Model:
                 m.p_full[g & 1].arrive()
                 yield
             yield from m.wait_last_pv(G + n - 1)
+            if not live:
+                G += n
+                continue
             assert not m.pv_pending, "epilogue read O with a P*V in flight"
             assert m.O_seg == k and m.O_count == n, \
                 f"epilogue of segment {k} read O of segment {m.O_seg} ({m.O_count} of {n} tiles)"
@@ -265,7 +278,7 @@ class Model:
                 assert m.slot[g % m.S] == g, "S MMA read a K slot holding another tile"
                 assert m.q_slot[k & 1] == k, "S MMA read a Q slot holding another segment"
                 assert not m.fp8 or m.q_conv[k & 1] == k, "S MMA read a Q slot not yet converted"
-                assert m.S_read, "S buffer overwritten before the softmax copied it"
+                assert len(m.S_read_by) == NSM, "S buffer overwritten before the softmax copied it"
                 m.q_reads[k & 1] += 1
             else:
                 _, g, k, acc = op
@@ -286,7 +299,7 @@ class Model:
         m.pipe.pop(0)
         if op[0] == "S":
             _, g, k = op
-            m.S_buf, m.S_read = g, False
+            m.S_buf, m.S_read_by = g, set()
             m.readers[g].discard("S")
             m.q_reads[k & 1] -= 1
         else:
@@ -303,7 +316,7 @@ class Model:
     # --------------------------------------------------------------- run
     def run(self):
         m = self
-        roles = [self.producer(), self.mma(), self.softmax()]
+        roles = [self.producer(), self.mma()] + [self.softmax(r) for r in range(NSM)]
         if m.fp8:
             roles.append(self.converter())
         alive = list(roles)
@@ -438,7 +451,7 @@ def test_model_catches_a_late_q_release():
 
 def test_model_reports_a_deadlock():
     class Stuck(Model):
-        def softmax(self):
+        def softmax(self, role=0):
             while True:
                 yield WAIT
     with pytest.raises(AssertionError, match="deadlock"):
@@ -461,3 +474,29 @@ def test_model_catches_an_unconverted_q_read():
             caught = True
             break
     assert caught
+
+
+def test_model_catches_an_early_p_arrival_of_the_padding_warps():
+    # a padding-row warp that arrives on P buffer g % 2 before waiting for
+    # S(g) can complete that buffer's phase before the query-row warp wrote
+    # P(g), so P(g) V_g runs on a P buffer holding another tile
+    class EarlyPad(Model):
+        def softmax(self, role=0):
+            if role == 0:
+                yield from Model.softmax(self, role)
+                return
+            m = self
+            G = 0
+            for k, n in enumerate(m.segs):
+                for j in range(n):
+                    g = G + j
+                    m.p_full[g & 1].arrive()
+                    yield
+                    while not m.s_full.ready(g):
+                        yield WAIT
+                    m.S_read_by.add(role)
+                    m.s_free.arrive()
+                    yield
+                yield from m.wait_last_pv(G + n - 1)
+                G += n
+    assert _run_mutant(EarlyPad, 41)
